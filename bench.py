@@ -1,0 +1,401 @@
+"""Benchmark of the routed-MoE FFN layer on GB300 (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline]
+
+A step is one pass of the whole layer (router + top-k, permutation, gate/up
+GEMM with SwiGLU, down GEMM, unpermutation with the shared expert) over one
+batch of T tokens of a seeded synthetic workload; the default is the
+decode-shaped layer (T=128, D=4096, 512 experts of intermediate 1024, top-10,
+one shared expert, bf16).  Expert weights (12.9 GB) dwarf the 129 MB L2, so
+no flush is needed between steps.  With N > 1 (torchrun) every rank runs an
+independent replica of the layer on its own GPU (the layer needs no
+exchange); `value` counts the tokens of all ranks over the slowest rank's
+time.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the workload per step); it is the baseline the pages'
+method is checked against, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_moe_expert_02_gb300 import MoELayer, synth  # noqa: E402
+from sparse_moe_expert_02_gb300 import _lib as L  # noqa: E402
+
+STAGES = ("route", "permute", "gemm_gateup", "gemm_down", "unpermute")
+KERNEL_FILES = {"gemm_gateup": "gemm_tc.cu", "gemm_down": "gemm_tc.cu"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = f"/tmp/moe_clocks_{os.getpid()}.csv"
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[2 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def algorithmic(shape, counts: np.ndarray):
+    """Bytes and flops the method itself must move and compute (no padding,
+    no intermediate round trips): touched routed experts + shared expert +
+    router weight, x in, out, and the routing blob."""
+    D, E, I, k, T = shape.D, shape.E, shape.I, shape.top_k, shape.T
+    bw = {"f32": 4, "bf16": 2, "fp8": 1}[shape.dtype]
+    bx = 4 if shape.dtype == "f32" else 2
+    touched = int((counts[:E] > 0).sum())
+    scale_bytes = (3 * (I // 128) * (D // 128) * 4) if shape.dtype == "fp8" else 0
+    per_expert = 3 * D * I * bw + scale_bytes
+    layer_bytes = (touched + 1) * per_expert + E * D * bx + T * D * bx + T * D * 4 + 8 * T * k
+    flops = T * (2 * D * E + (k + 1) * 6 * D * I)
+    gu_bytes = (touched + 1) * (2 * I * D * bw + 2 * scale_bytes // 3) + (T * k + T) * D * bw + (T * k + T) * I * bw
+    dn_bytes = (touched + 1) * (D * I * bw + scale_bytes // 3) + (T * k + T) * I * bw + (T * k + T) * D * 2
+    return {"touched_experts": touched, "layer_bytes": layer_bytes, "flops": flops,
+            "gemm_gateup_bytes": gu_bytes, "gemm_down_bytes": dn_bytes,
+            "gemm_gateup_flops": (T * k + T) * 4 * D * I, "gemm_down_flops": (T * k + T) * 2 * D * I,
+            "per_expert_bytes": per_expert}
+
+
+def traffic_for(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the kernel source as it stands now (else null)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        ent = d[workload][kernel]
+        src = os.path.join(ROOT, "sparse_moe_expert_02_gb300", "csrc", ent["source_file"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        return ent["dram_bytes_per_launch"] if h == ent["source_sha"] else None
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ ours
+
+def run_ours(args, shape, world, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    inp = synth.make_inputs(shape, seed=args.seed, device=dev)
+    layer = MoELayer.from_shape(shape, inp, device=local)
+    # inputs the layer no longer needs (FP8: the fp32 originals)
+    if shape.dtype == "fp8":
+        for n in ("w_gate", "w_up", "w_down"):
+            inp[n] = None
+        torch.cuda.empty_cache()
+    x = inp["x"]
+    T = shape.T
+    out = layer.new_out(T)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        layer.forward(x, out)
+    layer.check()
+    counts = layer.views(T)["counts"].cpu().numpy()
+    alg = algorithmic(shape, counts)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(args.steps)]
+    l0 = L.moe_launch_count()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for s in range(args.steps):
+            e = ev[s]
+            e[0].record(stream)
+            layer.init_ws()
+            layer.route(x)
+            e[1].record(stream)
+            layer.permute(x)
+            e[2].record(stream)
+            layer.gemm_gateup(x)
+            e[3].record(stream)
+            layer.gemm_down(T)
+            e[4].record(stream)
+            layer.unpermute(T, out)
+            e[5].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+    launches = L.moe_launch_count() - l0
+    layer.check()
+    ms_local = t_start.elapsed_time(t_end)
+    stage_ms = {st: statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps))
+                for i, st in enumerate(STAGES)}
+    ms = ms_local
+    if world > 1:
+        t = torch.tensor([ms_local], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+        torch.distributed.barrier()
+    ms_per_step = ms / args.steps
+    value = world * T * args.steps / (ms / 1e3)
+
+    # end to end through the public call, host buffers, copies inside the timing
+    x_h = x.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    x_d = torch.empty_like(x)
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x_d.copy_(x_h, non_blocking=True)
+        layer.forward(x_d, out)
+        out_h.copy_(out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(a.elapsed_time(b))
+    layer.check()
+    e2e_ms_step = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([e2e_ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms_step = float(t.item())
+
+    peaks = load_peaks()
+    dom = max(("gemm_gateup", "gemm_down"), key=lambda s: stage_ms[s])
+    hbm_bound = shape.dtype != "fp8" or shape.T <= 2048
+    if hbm_bound:
+        achieved = alg[dom + "_bytes"] / (stage_ms[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    else:
+        achieved = alg[dom + "_flops"] / (stage_ms[dom] / 1e3) / 1e12
+        pk = peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]
+        pk = pk * (2.0 if shape.dtype == "fp8" else 1.0)
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk, "unit": "TFLOP/s",
+                "frac": round(achieved / pk, 4)}
+    roof["kernel"] = dom
+    roof["traffic"] = traffic_for(dom, shape.name)
+    roof["peak_source"] = peaks["source"]
+    layer_gbs = alg["layer_bytes"] / (ms_per_step / 1e3) / 1e9
+    res = {
+        "metric": "routed-MoE layer tokens/s at E=512,k=10,D=4096",
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {"f32": "f32", "bf16": "bf16", "fp8": "e4m3"}[shape.dtype],
+        "data": "synthetic (seeded; random-init weights of the layer's shape)",
+        "config": {"workload": shape.name, "T": T, "D": shape.D, "E": shape.E, "I": shape.I,
+                   "top_k": shape.top_k, "shared_experts": 1, "router_bias_zipf_s": shape.zipf_s,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (expert weights stream from HBM every step)",
+                   "touched_experts": alg["touched_experts"]},
+        "roofline": roof,
+        "layer_roofline": {"bound": "hbm", "achieved": round(layer_gbs, 1), "peak": peaks["hbm_gbs"],
+                           "unit": "GB/s", "frac": round(layer_gbs / peaks["hbm_gbs"], 4),
+                           "alg_bytes": alg["layer_bytes"], "alg_flops": alg["flops"],
+                           "tflops": round(alg["flops"] / (ms_per_step / 1e3) / 1e12, 2)},
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "e2e": {"value": round(world * T / (e2e_ms_step / 1e3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": out.numel() * out.element_size()},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+        "impl": "ours",
+        "gemm_path": "tcgen05" if "tcgen05" in L.moe_build_info() else "simt",
+    }
+    return res, inp, layer
+
+
+# ------------------------------------------------------------ oracle leg
+
+def oracle_sample(shape, inp, n_tokens: int, seed: int = 1):
+    """Time the fp64 oracle on n_tokens of the workload: its own router
+    (fp64 logits, top-k) and every chosen expert plus the shared one."""
+    import oracle
+    g = np.random.default_rng(seed)
+    rows = np.sort(g.choice(shape.T, size=min(n_tokens, shape.T), replace=False))
+    x = inp["x"][torch.as_tensor(rows, device=inp["x"].device)].cpu()
+    wr = inp["w_router"].cpu()
+    b = inp["b_router"].cpu() if shape.has_bias else None
+    t0 = time.perf_counter()
+    z = oracle.logits(x, wr, b)
+    idx, w = oracle.topk(z, shape.top_k)
+    t_route = time.perf_counter() - t0
+    used = np.unique(idx)
+    groups = torch.as_tensor(np.concatenate([used, [shape.E]]), dtype=torch.long)
+    remap = np.full(shape.E, -1, np.int64)
+    remap[used] = np.arange(len(used))
+    idx_sub = remap[idx].astype(np.int32)
+
+    def take(n):
+        t = inp[n]
+        return t.index_select(0, groups.to(t.device)).cpu()
+
+    if shape.dtype == "fp8":
+        ex = oracle.Experts.quantised(take("w_gate"), take("w_up"), take("w_down"))
+    else:
+        ex = oracle.Experts(shape.dtype, take("w_gate"), take("w_up"), take("w_down"))
+    t1 = time.perf_counter()
+    oracle.moe_tokens(x, idx_sub, w, ex)
+    t_exp = time.perf_counter() - t1
+    return len(rows), t_route + t_exp
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args, shape, world, rank, local):
+    """The fp64 CPU oracle, timed as it stands on the host cores."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
+    inp = synth.make_inputs(shape, seed=args.seed, device=dev)
+    n = args.ref_tokens
+    times = []
+    for i in range(args.warmup + args.steps):
+        ntok, dt = oracle_sample(shape, inp, n, seed=100 + i)
+        if i >= args.warmup:
+            times.append(dt)
+    ms = sum(times) * 1e3
+    value = ntok * args.steps / (ms / 1e3)
+    cores = int(os.environ.get("OMP_NUM_THREADS", cpu_cores()))
+    sample = f"{ntok} of {shape.T} tokens per step, whole layer in fp64 (router, top-k, {shape.top_k} experts + shared)"
+    return {
+        "metric": "routed-MoE layer tokens/s at E=512,k=10,D=4096",
+        "value": round(value, 3), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": shape.name, "T": shape.T, "D": shape.D, "E": shape.E, "I": shape.I,
+                   "top_k": shape.top_k},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=synth.DECODE_BF16.name, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=24, help="oracle sample size for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per step for --impl reference")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    shape = synth.WORKLOADS[args.workload]
+    world, rank, local = dist_env()
+    if world > 1:
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            torch.cuda.set_device(local)
+        torch.distributed.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, shape, world, rank, local)
+            if res is not None:
+                print(json.dumps(res), flush=True)
+            return
+        res, inp, layer = run_ours(args, shape, world, rank, local)
+        if rank == 0 and not args.no_cpu_baseline:
+            import oracle
+            oracle.build()
+            ntok, dt = oracle_sample(shape, inp, args.cpu_tokens)
+            res["cpu_baseline"] = {"value": round(ntok / dt, 3), "unit": "tokens/s",
+                                   "cores": int(os.environ.get("OMP_NUM_THREADS", cpu_cores())), "kind": "oracle",
+                                   "sample": f"{ntok} of {shape.T} tokens, whole layer in fp64 "
+                                             f"(router, top-k, {shape.top_k} experts + shared), {dt:.1f} s"}
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

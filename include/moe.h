@@ -1,0 +1,226 @@
+/*
+ * moe.h -- C ABI of libmoe, a single-GPU (sm_103a) routed Mixture-of-Experts
+ * FFN layer.
+ *
+ * The layer ("Systems engineering playbook: Qwen 3.5 MoE on Ironwood TPU",
+ * English page, section "The Architectural Constraints That Break Naive
+ * Sharding"; aihot.vn translation of the report, section 1.3 "Sparse
+ * Mixture-of-Experts"): a router gate scores every token against E experts,
+ * the top_k experts are chosen through a softmax distribution and their
+ * weights renormalised, each chosen SwiGLU expert runs on the token, and an
+ * always-on shared expert is added:
+ *
+ *     z      = x W_r^T + b                       (router logits, fp32)
+ *     idx, w = top_k(z), softmax over the chosen z
+ *     out[t] = shared(x_t) + sum_j w[t,j] * expert_{idx[t,j]}(x_t)
+ *     expert_g(v) = W_down_g ( silu(W_gate_g v) * (W_up_g v) )
+ *
+ * Ties between equal logits go to the lower expert index; output slots are
+ * ordered by descending logit.  Expert indices and weights are kept as one
+ * int32 "blob" of two [T, top_k] planes (plane 0 the index, plane 1 the fp32
+ * bit pattern of the weight), the packing of the English page's section
+ * "Fusing Three Collectives Into Two".
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers on the plan's device, owned by
+ *     the caller, at least 16-byte aligned, row-major and dense.  The library
+ *     allocates no device memory; it uses the caller's workspace.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call only enqueues work: nothing synchronises the host,
+ *     so a sequence of calls can be captured into a CUDA graph.
+ *   - Argument errors are returned synchronously before anything is enqueued.
+ *     MOE_ERR_CUDA means a launch failed.  Conditions found on the device (a
+ *     bounded wait that ran out, a non-finite router logit, an index out of
+ *     range) are recorded in an error word inside the workspace and reported
+ *     by moe_check().  No entry point prints, exits or traps.
+ *   - A workspace must not be used by two calls in flight at the same time.
+ *
+ * Weight layout (E+1 groups; group E is the shared expert, whose
+ * intermediate size equals I):
+ *   w_router [E, D]         fp32 (MOE_F32 layer) or bf16 (all others)
+ *   b_router [E]            fp32, or NULL when has_router_bias == 0
+ *   w_gate   [E+1, I, D]    fp32 | bf16 | E4M3 codes (uint8)
+ *   w_up     [E+1, I, D]    same
+ *   w_down   [E+1, D, I]    same
+ *   s_gate, s_up [E+1, I/128, D/128] and s_down [E+1, D/128, I/128]:
+ *                           fp32 block scales, MOE_FP8_E4M3_B128 only.
+ * Every matrix is [out_features, in_features]: the reduction dimension is
+ * innermost (K-major), which is what the tensor-core operand loads want.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Every entry point is exported from the shared library. */
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,    /* NULL / misaligned pointer, T out of range */
+    MOE_ERR_UNSUPPORTED = 2,    /* shape or dtype this build has no kernel for */
+    MOE_ERR_WORKSPACE = 3,      /* workspace smaller than moe_workspace_size() */
+    MOE_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
+    MOE_ERR_DEVICE_TIMEOUT = 5, /* a bounded device wait ran out (moe_check) */
+    MOE_ERR_BOUNDS = 6,         /* a device-side index check failed (moe_check) */
+    MOE_ERR_NONFINITE = 7       /* a router logit was NaN or infinite (moe_check) */
+} moe_status;
+
+/* Arithmetic type of the layer.
+ *   MOE_F32: fp32 activations and weights, fp32 arithmetic throughout (no
+ *     tensor cores).
+ *   MOE_BF16: bf16 x, weights and intermediates (permuted x, h, expert
+ *     outputs), fp32 accumulation, fp32 or bf16 output.
+ *   MOE_FP8_E4M3_B128: expert weights as E4M3 codes with one fp32 scale per
+ *     128x128 block; both expert GEMM inputs (x and h) quantised to E4M3 per
+ *     token per 128-column group with s = amax/448 and
+ *     code = E4M3_rne_satfinite(fp32(v * fp32(448/amax))); fp32 accumulation
+ *     with the block scales applied per 128-wide K chunk; router in bf16;
+ *     bf16 or fp32 output. */
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2 } moe_dtype;
+
+/* moe_config.flags */
+#define MOE_FLAG_FORCE_SIMT 0x1u   /* expert GEMMs on the CUDA-core kernel (cross-check path) */
+
+typedef struct moe_config {
+    int32_t T_max;           /* largest token count a call may pass */
+    int32_t D, E, I, top_k;  /* hidden size, routed experts, intermediate, experts per token */
+    int32_t dtype;           /* moe_dtype */
+    int32_t out_dtype;       /* MOE_F32 or MOE_BF16 */
+    int32_t has_router_bias; /* 1: b_router is added to the logits */
+    uint32_t flags;          /* MOE_FLAG_* */
+    int64_t spin_limit_ns;   /* bound on every device-side wait; 0 = 2 s */
+} moe_config;
+
+typedef struct moe_weights {
+    const void* w_router;
+    const float* b_router;
+    const void* w_gate;
+    const void* w_up;
+    const void* w_down;
+    const float* s_gate;
+    const float* s_up;
+    const float* s_down;
+} moe_weights;
+
+typedef struct moe_plan moe_plan;
+
+/* Byte offsets of the workspace's parts for T tokens (all 256-byte aligned).
+ * Stage entry points read and write these parts; tests may inspect them.
+ * Rows of the expert-contiguous layout: routed pairs first (T*top_k rows,
+ * grouped by expert), then the T rows of the shared expert. */
+typedef struct moe_ws_layout {
+    size_t total;      /* bytes needed */
+    size_t err;        /* uint32[4]: first error code, then three diagnostic words */
+    size_t logits;     /* f32 [T, E] router logits (bias included) */
+    size_t blob;       /* int32 [2, T, top_k]: expert index plane, fp32-weight-bits plane */
+    size_t counts;     /* int32 [E+1]: rows per group; counts[E] = T */
+    size_t offsets;    /* int32 [E+2]: exclusive prefix of counts; offsets[E] = T*top_k */
+    size_t tiles;      /* int32 [E+2]: exclusive prefix of ceil(counts/128) (row tiles) */
+    size_t inv;        /* int32 [T*top_k]: row of pair (t, j) in the grouped layout */
+    size_t src_tok;    /* int32 [T*top_k + T]: token of each grouped row */
+    size_t hist;       /* int32 [chunks, E]: per-chunk expert histograms (scratch) */
+    size_t xq;         /* FP8: E4M3 [T, D] quantised x */
+    size_t xq_scale;   /* FP8: f32 [T, D/128] */
+    size_t xp;         /* [T*top_k, D] x gathered into grouped order (layer dtype; E4M3 for FP8) */
+    size_t xp_scale;   /* FP8: f32 [T*top_k, D/128] */
+    size_t h;          /* [T*top_k + T, I] SwiGLU activations (f32 | bf16 | E4M3) */
+    size_t h_scale;    /* FP8: f32 [T*top_k + T, I/128] */
+    size_t y;          /* [T*top_k + T, D] expert outputs (f32 for MOE_F32, else bf16) */
+} moe_ws_layout;
+
+/* Validate a configuration and build a host-side plan for `device`.
+ * Supported: D, I multiples of 128 (64 for MOE_F32), E <= 1024,
+ * 1 <= top_k <= min(E, 32), 1 <= T_max <= 2^20, T_max*(top_k+1) < 2^31.
+ * The plan owns no device memory.  *out is NULL on error. */
+MOE_API moe_status moe_plan_create(const moe_config* cfg, int device, moe_plan** out);
+MOE_API void moe_plan_destroy(moe_plan* plan);
+MOE_API const moe_config* moe_plan_config(const moe_plan* plan);
+
+/* Workspace layout / size for T tokens (1 <= T <= T_max). */
+MOE_API moe_status moe_workspace_layout(const moe_plan* plan, int32_t T, moe_ws_layout* out);
+MOE_API moe_status moe_workspace_size(const moe_plan* plan, int32_t T, size_t* bytes);
+
+/* Zero the workspace's error word (moe_forward does this itself). */
+MOE_API moe_status moe_workspace_init(const moe_plan* plan, void* ws, size_t ws_bytes, void* stream);
+
+/* Block-quantise fp32 weights to E4M3 (English page, "Roofline Validation":
+ * FP8 scaling blocks audited against a higher-precision path).  w is
+ * [groups, rows, cols] fp32; q receives [groups, rows, cols] E4M3 codes and s
+ * [groups, rows/128, cols/128] fp32 scales, s = amax/448 of each 128x128
+ * block (1 for an all-zero block).  rows and cols must be multiples of 128. */
+MOE_API moe_status moe_quantize_weights(const moe_plan* plan, const float* w, int64_t groups, int32_t rows,
+                                int32_t cols, uint8_t* q, float* s, void* stream);
+
+/* The whole layer: route, permute, gate/up GEMM with SwiGLU, down GEMM,
+ * unpermute with the shared-expert add.  x [T, D] (fp32 for MOE_F32, else
+ * bf16); out [T, D] of cfg.out_dtype.  blob_out (nullable) receives a copy of
+ * the [2, T, top_k] routing blob; logits_out (nullable) a copy of the [T, E]
+ * fp32 logits.  Clears the workspace error word first. */
+MOE_API moe_status moe_forward(const moe_plan* plan, const moe_weights* w, const void* x, int32_t T, void* out,
+                       int32_t* blob_out, float* logits_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Stage entry points: the same kernels moe_forward runs, one stage per call,
+ * reading and writing the workspace parts named in moe_ws_layout. */
+
+/* Router GEMM (logits, bias added) then moe_topk. */
+MOE_API moe_status moe_route(const moe_plan* plan, const moe_weights* w, const void* x, int32_t T, void* ws,
+                     size_t ws_bytes, void* stream);
+/* From ws.logits: top_k with lowest-index tie-break, softmax over the chosen
+ * logits, written into ws.blob.  Non-finite logits set MOE_ERR_NONFINITE. */
+MOE_API moe_status moe_topk(const moe_plan* plan, int32_t T, void* ws, size_t ws_bytes, void* stream);
+/* From ws.blob plane 0: counts, offsets, tiles, inv, src_tok (a stable
+ * counting sort of the (t, j) pairs in row-major order), and xp = x rows in
+ * grouped order (quantised to E4M3 for the FP8 layer, with xq for the shared
+ * group). */
+MOE_API moe_status moe_permute(const moe_plan* plan, const void* x, int32_t T, void* ws, size_t ws_bytes,
+                       void* stream);
+/* h[r] = silu(W_gate_g a_r) * (W_up_g a_r) for every grouped row r of group g,
+ * a_r = xp[r] for routed rows and x[t] for the shared group. */
+MOE_API moe_status moe_gemm_gateup(const moe_plan* plan, const moe_weights* w, const void* x, int32_t T, void* ws,
+                           size_t ws_bytes, void* stream);
+/* y[r] = W_down_g h[r]. */
+MOE_API moe_status moe_gemm_down(const moe_plan* plan, const moe_weights* w, int32_t T, void* ws, size_t ws_bytes,
+                         void* stream);
+/* out[t] = y[T*top_k + t] + sum_j w[t,j] * y[inv[t*top_k + j]], fp32
+ * accumulation in slot order (English page, table in "Pallas Kernels,
+ * SparseCore Co-Design, and the Roofline": token unpermutation plus the local
+ * reduction). */
+MOE_API moe_status moe_unpermute(const moe_plan* plan, int32_t T, void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, read the workspace error word and return the first
+ * device-side error recorded since the last clear (MOE_OK if none). */
+MOE_API moe_status moe_check(const moe_plan* plan, const void* ws, void* stream);
+
+/* Self-test of the bounded-wait machinery: one block waits on an mbarrier
+ * that nothing arrives at, for at most limit_ns, then records
+ * MOE_ERR_DEVICE_TIMEOUT in the error word and returns normally. */
+MOE_API moe_status moe_selftest_wait_timeout(const moe_plan* plan, void* ws, size_t ws_bytes, int64_t limit_ns,
+                                     void* stream);
+
+MOE_API const char* moe_status_str(moe_status s);
+
+/* Human-readable detail of the last error returned on this host thread
+ * (which argument, which CUDA call); empty if none. */
+MOE_API const char* moe_last_error_detail(void);
+
+/* Number of kernels this library has launched in this process (all
+ * devices, all streams), for launch accounting by benchmarks. */
+MOE_API uint64_t moe_launch_count(void);
+
+/* Build identification: "sm_103a tcgen05" plus the kernel set compiled in. */
+MOE_API const char* moe_build_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

@@ -1,0 +1,407 @@
+// C ABI of libmoe: argument validation, workspace carving and the launch
+// sequence of the routed-MoE layer.  Every entry point only enqueues work on
+// the caller's stream; the only host synchronisation is in moe_check().
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+}  // namespace moe
+
+struct moe_plan {
+    moe_config cfg;
+    int device;
+    int num_sms;
+    int64_t spin_ns;
+};
+
+namespace {
+
+thread_local char g_detail[256];
+
+moe_status cuda_fail(cudaError_t e, const char* where) {
+    snprintf(g_detail, sizeof(g_detail), "%s: %s", where, cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+}
+moe_status arg_fail(moe_status s, const char* what) {
+    snprintf(g_detail, sizeof(g_detail), "%s", what);
+    return s;
+}
+#define MOE_CUDA(call)                                        \
+    do {                                                      \
+        cudaError_t e_ = (call);                              \
+        if (e_ != cudaSuccess) return cuda_fail(e_, #call);   \
+    } while (0)
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+int act_bytes(int dtype) { return dtype == MOE_F32 ? 4 : (dtype == MOE_BF16 ? 2 : 1); }
+int act_elem(int dtype) { return dtype == MOE_F32 ? moe::kF32 : (dtype == MOE_BF16 ? moe::kBF16 : moe::kE4M3); }
+int in_elem(int dtype) { return dtype == MOE_F32 ? moe::kF32 : moe::kBF16; }  // x and router
+
+void layout(const moe_config& c, int T, moe_ws_layout* L) {
+    const int64_t TK = (int64_t)T * c.top_k, R = TK + T;
+    const bool fp8 = c.dtype == MOE_FP8_E4M3_B128;
+    const int ab = act_bytes(c.dtype);
+    const int64_t nch = moe::cdiv(TK, moe::kPermChunk);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o += up256(bytes); return at; };
+    memset(L, 0, sizeof(*L));
+    L->err = take(16);
+    L->logits = take((size_t)T * c.E * 4);
+    L->blob = take((size_t)2 * TK * 4);
+    L->counts = take((size_t)(c.E + 1) * 4);
+    L->offsets = take((size_t)(c.E + 2) * 4);
+    L->tiles = take((size_t)(c.E + 2) * 4);
+    L->inv = take((size_t)TK * 4);
+    L->src_tok = take((size_t)R * 4);
+    L->hist = take((size_t)nch * c.E * 4);
+    L->xq = fp8 ? take((size_t)T * c.D) : 0;
+    L->xq_scale = fp8 ? take((size_t)T * (c.D / 128) * 4) : 0;
+    L->xp = take((size_t)TK * c.D * ab);
+    L->xp_scale = fp8 ? take((size_t)TK * (c.D / 128) * 4) : 0;
+    L->h = take((size_t)R * c.I * ab);
+    L->h_scale = fp8 ? take((size_t)R * (c.I / 128) * 4) : 0;
+    L->y = take((size_t)R * c.D * (c.dtype == MOE_F32 ? 4 : 2));
+    L->total = o;
+}
+
+struct Ws {
+    moe_ws_layout L;
+    char* base;
+    template <typename T> T* at(size_t off) const { return (T*)(base + off); }
+};
+
+moe_status check_call(const moe_plan* p, int32_t T, void* ws, size_t ws_bytes, Ws* out) {
+    if (!p) return arg_fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+    if (T < 1 || T > p->cfg.T_max) return arg_fail(MOE_ERR_INVALID_ARG, "T outside [1, T_max]");
+    if (!ws || !aligned(ws, 256)) return arg_fail(MOE_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+    layout(p->cfg, T, &out->L);
+    if (ws_bytes < out->L.total) return arg_fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_workspace_size()");
+    out->base = (char*)ws;
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != p->device)
+        return arg_fail(MOE_ERR_INVALID_ARG, "current CUDA device is not the plan's device");
+    return MOE_OK;
+}
+
+bool ptr_ok(const void* q) { return q != nullptr && aligned(q, 16); }
+
+moe_status check_weights(const moe_plan* p, const moe_weights* w, bool router, bool experts) {
+    if (!w) return arg_fail(MOE_ERR_INVALID_ARG, "weights is NULL");
+    if (router) {
+        if (!ptr_ok(w->w_router)) return arg_fail(MOE_ERR_INVALID_ARG, "w_router NULL or misaligned");
+        if (p->cfg.has_router_bias && !ptr_ok(w->b_router))
+            return arg_fail(MOE_ERR_INVALID_ARG, "b_router NULL or misaligned");
+    }
+    if (experts) {
+        if (!ptr_ok(w->w_gate) || !ptr_ok(w->w_up) || !ptr_ok(w->w_down))
+            return arg_fail(MOE_ERR_INVALID_ARG, "expert weight NULL or misaligned");
+        if (p->cfg.dtype == MOE_FP8_E4M3_B128 && (!ptr_ok(w->s_gate) || !ptr_ok(w->s_up) || !ptr_ok(w->s_down)))
+            return arg_fail(MOE_ERR_INVALID_ARG, "FP8 block scales NULL or misaligned");
+    }
+    return MOE_OK;
+}
+
+bool use_tc(const moe_plan* p, const moe::GroupedGemm& g) {
+    if (p->cfg.flags & MOE_FLAG_FORCE_SIMT) return false;
+    return moe::gemm_tc_supported(g);
+}
+
+moe_status run_gemm(const moe_plan* p, const moe::GroupedGemm& g, cudaStream_t s, const char* what) {
+    if (use_tc(p, g)) {
+        MOE_CUDA(moe::launch_gemm_tc(g, p->num_sms, s));
+        return MOE_OK;
+    }
+    if (g.elem == moe::kE4M3) return arg_fail(MOE_ERR_UNSUPPORTED, "FP8 GEMM shape without a tensor-core kernel");
+    cudaError_t e = moe::launch_gemm_simt(g, s);
+    if (e != cudaSuccess) return cuda_fail(e, what);
+    return MOE_OK;
+}
+
+int grouped_max_tiles(const moe_config& c, int T) {
+    const int64_t R = (int64_t)T * (c.top_k + 1);
+    return (int)(R / moe::kRowTile + c.E + 2);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_str(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_BOUNDS: return "device index check failed";
+        case MOE_ERR_NONFINITE: return "non-finite router logit";
+    }
+    return "unknown status";
+}
+
+const char* moe_last_error_detail(void) { return g_detail; }
+
+uint64_t moe_launch_count(void) { return moe::g_launches.load(std::memory_order_relaxed); }
+
+const char* moe_build_info(void) { return "libmoe sm_103a: tcgen05+TMA grouped GEMM, SIMT grouped GEMM, route/permute/unpermute"; }
+
+moe_status moe_plan_create(const moe_config* cfg, int device, moe_plan** out) {
+    if (!out) return arg_fail(MOE_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!cfg) return arg_fail(MOE_ERR_INVALID_ARG, "cfg is NULL");
+    const moe_config& c = *cfg;
+    if (c.dtype < MOE_F32 || c.dtype > MOE_FP8_E4M3_B128) return arg_fail(MOE_ERR_UNSUPPORTED, "dtype");
+    if (c.out_dtype != MOE_F32 && c.out_dtype != MOE_BF16) return arg_fail(MOE_ERR_UNSUPPORTED, "out_dtype");
+    if (c.E < 1 || c.E > 1024) return arg_fail(MOE_ERR_UNSUPPORTED, "E outside [1, 1024]");
+    if (c.top_k < 1 || c.top_k > std::min(c.E, 32)) return arg_fail(MOE_ERR_UNSUPPORTED, "top_k outside [1, min(E,32)]");
+    if (c.T_max < 1 || c.T_max > (1 << 20)) return arg_fail(MOE_ERR_UNSUPPORTED, "T_max outside [1, 2^20]");
+    if ((int64_t)c.T_max * (c.top_k + 1) >= (int64_t)1 << 31) return arg_fail(MOE_ERR_UNSUPPORTED, "T_max*(top_k+1) >= 2^31");
+    const int q = (c.dtype == MOE_F32) ? 64 : 128;
+    if (c.D < q || c.D % q || c.I < q || c.I % q) return arg_fail(MOE_ERR_UNSUPPORTED, "D and I must be multiples of 128 (64 for fp32)");
+    if (c.D > 65536 || c.I > 65536) return arg_fail(MOE_ERR_UNSUPPORTED, "D or I above 65536");
+    if (c.spin_limit_ns < 0) return arg_fail(MOE_ERR_INVALID_ARG, "spin_limit_ns < 0");
+    int ndev = 0;
+    if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)
+        return arg_fail(MOE_ERR_INVALID_ARG, "no such CUDA device");
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return arg_fail(MOE_ERR_CUDA, "device query failed");
+    moe_plan* p = new moe_plan;
+    p->cfg = c;
+    p->device = device;
+    p->num_sms = sms;
+    p->spin_ns = c.spin_limit_ns ? c.spin_limit_ns : 2000000000LL;
+    *out = p;
+    return MOE_OK;
+}
+
+void moe_plan_destroy(moe_plan* p) { delete p; }
+
+const moe_config* moe_plan_config(const moe_plan* p) { return p ? &p->cfg : nullptr; }
+
+moe_status moe_workspace_layout(const moe_plan* p, int32_t T, moe_ws_layout* out) {
+    if (!p || !out) return arg_fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    if (T < 1 || T > p->cfg.T_max) return arg_fail(MOE_ERR_INVALID_ARG, "T outside [1, T_max]");
+    layout(p->cfg, T, out);
+    return MOE_OK;
+}
+
+moe_status moe_workspace_size(const moe_plan* p, int32_t T, size_t* bytes) {
+    if (!bytes) return arg_fail(MOE_ERR_INVALID_ARG, "bytes is NULL");
+    moe_ws_layout L;
+    moe_status s = moe_workspace_layout(p, T, &L);
+    if (s == MOE_OK) *bytes = L.total;
+    return s;
+}
+
+moe_status moe_workspace_init(const moe_plan* p, void* ws, size_t ws_bytes, void* stream) {
+    if (!p || !ws || !aligned(ws, 256) || ws_bytes < 256) return arg_fail(MOE_ERR_INVALID_ARG, "workspace");
+    MOE_CUDA(cudaMemsetAsync(ws, 0, 16, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status moe_quantize_weights(const moe_plan* p, const float* w, int64_t groups, int32_t rows, int32_t cols,
+                                uint8_t* q, float* s, void* stream) {
+    if (!p) return arg_fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+    if (!ptr_ok(w) || !ptr_ok(q) || !ptr_ok(s)) return arg_fail(MOE_ERR_INVALID_ARG, "NULL or misaligned pointer");
+    if (groups < 1 || rows < 128 || cols < 128 || rows % 128 || cols % 128)
+        return arg_fail(MOE_ERR_UNSUPPORTED, "rows and cols must be positive multiples of 128");
+    MOE_CUDA(moe::launch_quant_blocks(w, groups, rows, cols, q, s, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status moe_topk(const moe_plan* p, int32_t T, void* ws, size_t ws_bytes, void* stream) {
+    Ws W;
+    moe_status st = check_call(p, T, ws, ws_bytes, &W);
+    if (st != MOE_OK) return st;
+    const moe_config& c = p->cfg;
+    MOE_CUDA(moe::launch_topk(W.at<float>(W.L.logits), T, c.E, c.top_k, W.at<int32_t>(W.L.blob),
+                              W.at<uint32_t>(W.L.err), (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status moe_route(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, void* ws, size_t ws_bytes,
+                     void* stream) {
+    Ws W;
+    moe_status st = check_call(p, T, ws, ws_bytes, &W);
+    if (st != MOE_OK) return st;
+    if ((st = check_weights(p, w, true, false)) != MOE_OK) return st;
+    if (!ptr_ok(x)) return arg_fail(MOE_ERR_INVALID_ARG, "x NULL or misaligned");
+    const moe_config& c = p->cfg;
+    moe::GroupedGemm g = {};
+    g.G = 1;
+    g.shared_group = -1;
+    g.rows = T;
+    g.max_tiles = (int)moe::cdiv(T, moe::kRowTile);
+    g.N = c.E;
+    g.K = c.D;
+    g.elem = in_elem(c.dtype);
+    g.a = x;
+    g.b = w->w_router;
+    g.out = W.at<float>(W.L.logits);
+    g.out_elem = moe::kF32;
+    g.bias = c.has_router_bias ? w->b_router : nullptr;
+    g.err = W.at<uint32_t>(W.L.err);
+    g.spin_ns = p->spin_ns;
+    if ((st = run_gemm(p, g, (cudaStream_t)stream, "router GEMM")) != MOE_OK) return st;
+    return moe_topk(p, T, ws, ws_bytes, stream);
+}
+
+moe_status moe_permute(const moe_plan* p, const void* x, int32_t T, void* ws, size_t ws_bytes, void* stream) {
+    Ws W;
+    moe_status st = check_call(p, T, ws, ws_bytes, &W);
+    if (st != MOE_OK) return st;
+    if (!ptr_ok(x)) return arg_fail(MOE_ERR_INVALID_ARG, "x NULL or misaligned");
+    const moe_config& c = p->cfg;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int TK = T * c.top_k;
+    MOE_CUDA(moe::launch_permute_index(W.at<int32_t>(W.L.blob), T, c.E, c.top_k, W.at<int32_t>(W.L.hist),
+                                       W.at<int32_t>(W.L.counts), W.at<int32_t>(W.L.offsets),
+                                       W.at<int32_t>(W.L.tiles), W.at<int32_t>(W.L.inv), W.at<int32_t>(W.L.src_tok),
+                                       W.at<uint32_t>(W.L.err), s));
+    if (c.dtype == MOE_FP8_E4M3_B128) {
+        MOE_CUDA(moe::launch_quant_rows(x, moe::kBF16, T, c.D, W.at<uint8_t>(W.L.xq), W.at<float>(W.L.xq_scale), s));
+        MOE_CUDA(moe::launch_gather_rows(W.at<uint8_t>(W.L.xq), 1, c.D, W.at<int32_t>(W.L.src_tok), TK,
+                                         W.at<uint8_t>(W.L.xp), s));
+        MOE_CUDA(moe::launch_gather_rows(W.at<float>(W.L.xq_scale), 4, (int64_t)(c.D / 128) * 4,
+                                         W.at<int32_t>(W.L.src_tok), TK, W.at<float>(W.L.xp_scale), s));
+    } else {
+        const int eb = act_bytes(c.dtype);
+        MOE_CUDA(moe::launch_gather_rows(x, eb, (int64_t)c.D * eb, W.at<int32_t>(W.L.src_tok), TK,
+                                         W.at<char>(W.L.xp), s));
+    }
+    return MOE_OK;
+}
+
+moe_status moe_gemm_gateup(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, void* ws,
+                           size_t ws_bytes, void* stream) {
+    Ws W;
+    moe_status st = check_call(p, T, ws, ws_bytes, &W);
+    if (st != MOE_OK) return st;
+    if ((st = check_weights(p, w, false, true)) != MOE_OK) return st;
+    if (!ptr_ok(x)) return arg_fail(MOE_ERR_INVALID_ARG, "x NULL or misaligned");
+    const moe_config& c = p->cfg;
+    const bool fp8 = c.dtype == MOE_FP8_E4M3_B128;
+    moe::GroupedGemm g = {};
+    g.G = c.E + 1;
+    g.shared_group = c.E;
+    g.offsets = W.at<int32_t>(W.L.offsets);
+    g.tiles = W.at<int32_t>(W.L.tiles);
+    g.max_tiles = grouped_max_tiles(c, T);
+    g.N = c.I;
+    g.K = c.D;
+    g.elem = act_elem(c.dtype);
+    g.a = W.at<void>(W.L.xp);
+    g.a_shared = fp8 ? (const void*)W.at<uint8_t>(W.L.xq) : x;
+    g.a_scale = fp8 ? W.at<float>(W.L.xp_scale) : nullptr;
+    g.a_shared_scale = fp8 ? W.at<float>(W.L.xq_scale) : nullptr;
+    g.b = w->w_gate;
+    g.b2 = w->w_up;
+    g.b_scale = w->s_gate;
+    g.b2_scale = w->s_up;
+    g.out = W.at<void>(W.L.h);
+    g.out_elem = act_elem(c.dtype);
+    g.out_scale = fp8 ? W.at<float>(W.L.h_scale) : nullptr;
+    g.err = W.at<uint32_t>(W.L.err);
+    g.spin_ns = p->spin_ns;
+    return run_gemm(p, g, (cudaStream_t)stream, "gate/up GEMM");
+}
+
+moe_status moe_gemm_down(const moe_plan* p, const moe_weights* w, int32_t T, void* ws, size_t ws_bytes,
+                         void* stream) {
+    Ws W;
+    moe_status st = check_call(p, T, ws, ws_bytes, &W);
+    if (st != MOE_OK) return st;
+    if ((st = check_weights(p, w, false, true)) != MOE_OK) return st;
+    const moe_config& c = p->cfg;
+    const bool fp8 = c.dtype == MOE_FP8_E4M3_B128;
+    moe::GroupedGemm g = {};
+    g.G = c.E + 1;
+    g.shared_group = -1;
+    g.offsets = W.at<int32_t>(W.L.offsets);
+    g.tiles = W.at<int32_t>(W.L.tiles);
+    g.max_tiles = grouped_max_tiles(c, T);
+    g.N = c.D;
+    g.K = c.I;
+    g.elem = act_elem(c.dtype);
+    g.a = W.at<void>(W.L.h);
+    g.a_scale = fp8 ? W.at<float>(W.L.h_scale) : nullptr;
+    g.b = w->w_down;
+    g.b_scale = w->s_down;
+    g.out = W.at<void>(W.L.y);
+    g.out_elem = (c.dtype == MOE_F32) ? moe::kF32 : moe::kBF16;
+    g.err = W.at<uint32_t>(W.L.err);
+    g.spin_ns = p->spin_ns;
+    return run_gemm(p, g, (cudaStream_t)stream, "down GEMM");
+}
+
+moe_status moe_unpermute(const moe_plan* p, int32_t T, void* out, void* ws, size_t ws_bytes, void* stream) {
+    Ws W;
+    moe_status st = check_call(p, T, ws, ws_bytes, &W);
+    if (st != MOE_OK) return st;
+    if (!ptr_ok(out)) return arg_fail(MOE_ERR_INVALID_ARG, "out NULL or misaligned");
+    const moe_config& c = p->cfg;
+    MOE_CUDA(moe::launch_unpermute(W.at<void>(W.L.y), c.dtype == MOE_F32 ? moe::kF32 : moe::kBF16,
+                                   W.at<int32_t>(W.L.blob), W.at<int32_t>(W.L.inv), T, c.D, c.top_k, out,
+                                   c.out_dtype == MOE_F32 ? moe::kF32 : moe::kBF16, W.at<uint32_t>(W.L.err),
+                                   (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, void* out,
+                       int32_t* blob_out, float* logits_out, void* ws, size_t ws_bytes, void* stream) {
+    Ws W;
+    moe_status st = check_call(p, T, ws, ws_bytes, &W);
+    if (st != MOE_OK) return st;
+    if ((st = check_weights(p, w, true, true)) != MOE_OK) return st;
+    if (!ptr_ok(x) || !ptr_ok(out)) return arg_fail(MOE_ERR_INVALID_ARG, "x or out NULL or misaligned");
+    if ((blob_out && !aligned(blob_out, 16)) || (logits_out && !aligned(logits_out, 16)))
+        return arg_fail(MOE_ERR_INVALID_ARG, "blob_out or logits_out misaligned");
+    cudaStream_t s = (cudaStream_t)stream;
+    MOE_CUDA(cudaMemsetAsync(ws, 0, 16, s));
+    if ((st = moe_route(p, w, x, T, ws, ws_bytes, stream)) != MOE_OK) return st;
+    if ((st = moe_permute(p, x, T, ws, ws_bytes, stream)) != MOE_OK) return st;
+    if ((st = moe_gemm_gateup(p, w, x, T, ws, ws_bytes, stream)) != MOE_OK) return st;
+    if ((st = moe_gemm_down(p, w, T, ws, ws_bytes, stream)) != MOE_OK) return st;
+    if ((st = moe_unpermute(p, T, out, ws, ws_bytes, stream)) != MOE_OK) return st;
+    const moe_config& c = p->cfg;
+    if (blob_out)
+        MOE_CUDA(cudaMemcpyAsync(blob_out, W.at<int32_t>(W.L.blob), (size_t)2 * T * c.top_k * 4,
+                                 cudaMemcpyDeviceToDevice, s));
+    if (logits_out)
+        MOE_CUDA(cudaMemcpyAsync(logits_out, W.at<float>(W.L.logits), (size_t)T * c.E * 4, cudaMemcpyDeviceToDevice, s));
+    return MOE_OK;
+}
+
+moe_status moe_check(const moe_plan* p, const void* ws, void* stream) {
+    if (!p || !ws) return arg_fail(MOE_ERR_INVALID_ARG, "NULL argument");
+    uint32_t word[4] = {0, 0, 0, 0};
+    MOE_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+    MOE_CUDA(cudaMemcpy(word, ws, sizeof(word), cudaMemcpyDeviceToHost));
+    if (word[0] != 0) {
+        snprintf(g_detail, sizeof(g_detail), "device error %u (%s), info %u %u %u", word[0],
+                 moe_status_str((moe_status)word[0]), word[1], word[2], word[3]);
+        return (moe_status)word[0];
+    }
+    return MOE_OK;
+}
+
+moe_status moe_selftest_wait_timeout(const moe_plan* p, void* ws, size_t ws_bytes, int64_t limit_ns, void* stream) {
+    if (!p || !ws || !aligned(ws, 256) || ws_bytes < 256) return arg_fail(MOE_ERR_INVALID_ARG, "workspace");
+    if (limit_ns < 0 || limit_ns > 10000000000LL) return arg_fail(MOE_ERR_INVALID_ARG, "limit_ns outside [0, 10 s]");
+    MOE_CUDA(moe::launch_selftest_timeout((uint32_t*)ws, limit_ns, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
+}  // extern "C"

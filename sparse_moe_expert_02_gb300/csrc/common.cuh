@@ -1,0 +1,72 @@
+// Device-side helpers shared by the libmoe kernels: element conversions,
+// the workspace error word, and a nanosecond clock for bounded waits.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+typedef __nv_bfloat16 bf16;
+
+// ---------------------------------------------------------------- errors
+
+// The error word: [0] first error code (moe_status), [1..3] diagnostics.
+// The first writer wins; later errors are dropped.
+__device__ __forceinline__ void record_error(uint32_t* err, uint32_t code, uint32_t a = 0, uint32_t b = 0,
+                                             uint32_t c = 0) {
+    if (err == nullptr) return;
+    if (atomicCAS(err, 0u, code) == 0u) {
+        err[1] = a;
+        err[2] = b;
+        err[3] = c;
+        __threadfence();
+    }
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ----------------------------------------------------------- conversions
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(bf16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+
+// E4M3, round to nearest even, saturating to +-448.
+__device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
+    return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+__device__ __forceinline__ float e4m3_to_f32(uint8_t q) {
+    __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)q, __NV_E4M3);
+    return __half2float(__half(hr));
+}
+
+// SiLU(a) * u in fp32: a / (1 + e^-a) * u.
+__device__ __forceinline__ float swiglu(float a, float u) { return a / (1.0f + expf(-a)) * u; }
+
+__host__ __device__ constexpr int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Group of a row tile: tiles[g] <= tile < tiles[g+1] (tiles has G+1 entries,
+// nondecreasing).  Binary search, G <= 1025.
+__device__ __forceinline__ int find_group(const int32_t* tiles, int G, int tile) {
+    int lo = 0, hi = G;  // invariant: tiles[lo] <= tile < tiles[hi]
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (__ldg(tiles + mid) <= tile) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
+
+}  // namespace moe

@@ -1,0 +1,156 @@
+// Grouped GEMM on the CUDA cores (fp32 arithmetic), C_g = A_g * B_g^T.
+//
+// This is the kernel of the fp32 layer ("fp32 throughout": no tensor-core
+// rounding of the operands) and an independent cross-check of the
+// tensor-core path for bf16.  128 x 64 output tiles, K in steps of 16,
+// 256 threads each owning an 8 x 4 block (two of them for SwiGLU, whose
+// gate and up products share the A tile).  Row tiles of the grouped layout
+// are walked through the device-built tile prefix, so no host round trip
+// is needed to learn the per-expert row counts.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+namespace {
+constexpr int BM = 128, BN = 64, BK = 16;
+
+template <typename T> __device__ __forceinline__ void load8(const T* p, float* v);
+template <> __device__ __forceinline__ void load8<float>(const float* p, float* v) {
+    float4 a = __ldg((const float4*)p), b = __ldg((const float4*)(p + 4));
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+template <> __device__ __forceinline__ void load8<bf16>(const bf16* p, float* v) {
+    int4 r = __ldg((const int4*)p);
+    const bf16* e = (const bf16*)&r;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __bfloat162float(e[i]);
+}
+template <typename T> __device__ __forceinline__ void load4(const T* p, float* v) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = to_f32(p[i]);
+}
+}  // namespace
+
+template <typename TE, typename TO, bool SWIGLU>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(GroupedGemm g) {
+    __shared__ float As[BK][BM + 4];
+    __shared__ float Bs[BK][BN + 4];
+    __shared__ float Bs2[SWIGLU ? BK : 1][BN + 4];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int N = g.N, K = g.K;
+    const int n0 = blockIdx.y * BN;
+    const int total = g.offsets ? __ldg(g.tiles + g.G) : (int)cdiv(g.rows, BM);
+    const TE* A = (const TE*)g.a;
+    const TE* As_ = (const TE*)g.a_shared;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        int grp = 0, m0, nrows, out0;
+        if (g.offsets) {
+            grp = find_group(g.tiles, g.G, tile);
+            m0 = (tile - __ldg(g.tiles + grp)) * BM;
+            out0 = __ldg(g.offsets + grp);
+            nrows = __ldg(g.offsets + grp + 1) - out0;
+        } else {
+            m0 = tile * BM;
+            out0 = 0;
+            nrows = g.rows;
+        }
+        const TE* abase = (grp == g.shared_group) ? As_ : A + (int64_t)out0 * K;
+        const TE* b1 = (const TE*)g.b + (int64_t)grp * N * K;
+        const TE* b2 = SWIGLU ? (const TE*)g.b2 + (int64_t)grp * N * K : nullptr;
+        float acc[8][4], acc2[SWIGLU ? 8 : 1][4];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) { acc[i][j] = 0.f; if (SWIGLU) acc2[i][j] = 0.f; }
+        // loader coordinates
+        const int ar = tid >> 1, ak = (tid & 1) * 8;   // A: 128 rows x 16 k
+        const int br = tid >> 2, bk = (tid & 3) * 4;   // B: 64 rows x 16 k
+        const bool a_ok = (m0 + ar) < nrows;
+        const bool b_ok = (n0 + br) < N;
+        for (int k0 = 0; k0 < K; k0 += BK) {
+            float av[8], bv[4], bv2[4];
+            if (a_ok) load8<TE>(abase + (int64_t)(m0 + ar) * K + k0 + ak, av);
+            else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) av[i] = 0.f;
+            }
+            if (b_ok) {
+                load4<TE>(b1 + (int64_t)(n0 + br) * K + k0 + bk, bv);
+                if (SWIGLU) load4<TE>(b2 + (int64_t)(n0 + br) * K + k0 + bk, bv2);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) { bv[i] = 0.f; bv2[i] = 0.f; }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) As[ak + i][ar] = av[i];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                Bs[bk + i][br] = bv[i];
+                if (SWIGLU) Bs2[bk + i][br] = bv2[i];
+            }
+            __syncthreads();
+#pragma unroll
+            for (int kk = 0; kk < BK; ++kk) {
+                float a[8], b[4], b2v[4];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) a[i] = As[kk][ty * 8 + i];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    b[j] = Bs[kk][tx * 4 + j];
+                    if (SWIGLU) b2v[j] = Bs2[kk][tx * 4 + j];
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                        if (SWIGLU) acc2[i][j] = fmaf(a[i], b2v[j], acc2[i][j]);
+                    }
+            }
+        }
+        TO* out = (TO*)g.out;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int m = m0 + ty * 8 + i;
+            if (m >= nrows) continue;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int n = n0 + tx * 4 + j;
+                if (n >= N) continue;
+                float v = SWIGLU ? swiglu(acc[i][j], acc2[i][j]) : acc[i][j];
+                if (g.bias) v += __ldg(g.bias + n);
+                out[(int64_t)(out0 + m) * N + n] = from_f32<TO>(v);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_gemm_simt(const GroupedGemm& g, cudaStream_t stream) {
+    if (g.max_tiles <= 0) return cudaGetLastError();
+    dim3 grid((unsigned)std::min(g.max_tiles, 4096), (unsigned)cdiv(g.N, BN)), block(256);
+    const bool sw = g.b2 != nullptr;
+    if (g.elem == kF32) {
+        if (g.out_elem != kF32) return cudaErrorInvalidValue;
+        if (sw) gemm_simt_kernel<float, float, true><<<grid, block, 0, stream>>>(g);
+        else gemm_simt_kernel<float, float, false><<<grid, block, 0, stream>>>(g);
+    } else if (g.elem == kBF16) {
+        if (g.out_elem == kF32) {
+            if (sw) gemm_simt_kernel<bf16, float, true><<<grid, block, 0, stream>>>(g);
+            else gemm_simt_kernel<bf16, float, false><<<grid, block, 0, stream>>>(g);
+        } else {
+            if (sw) gemm_simt_kernel<bf16, bf16, true><<<grid, block, 0, stream>>>(g);
+            else gemm_simt_kernel<bf16, bf16, false><<<grid, block, 0, stream>>>(g);
+        }
+    } else {
+        return cudaErrorInvalidValue;
+    }
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,73 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kRowTile = 128;      // rows of the grouped layout per GEMM tile
+constexpr int kPermChunk = 1024;   // (t, j) pairs per permute chunk
+
+// Element kinds of the GEMM operands.
+enum Elem : int { kF32 = 0, kBF16 = 1, kE4M3 = 2 };
+
+// One grouped GEMM, C_g = A_g * B_g^T, over the groups of the expert-grouped
+// row layout (or a single dense group).
+//   rows of group g: offsets[g] .. offsets[g] + counts[g] - 1 of the output;
+//   A row r of group g comes from a[r] (routed groups) or a_shared[r - offsets[g]]
+//   (group == shared_group); B_g is b + g * N * K (and b2 likewise for the
+//   SwiGLU "up" matrix).
+struct GroupedGemm {
+    int G;                       // groups
+    int shared_group;            // group whose A rows come from a_shared (-1: none)
+    const int32_t* offsets;      // [G+1] device (nullptr: single group of `rows` rows)
+    const int32_t* tiles;        // [G+1] device prefix of ceil(rows/128) (nullptr with offsets)
+    int rows;                    // single-group row count
+    int max_tiles;               // host bound on the total number of row tiles
+    int N, K;
+    int elem;                    // Elem of A and B
+    const void* a;               // [*, K]
+    const void* a_shared;        // [*, K]
+    const float* a_scale;        // FP8: [*, K/128] per-row group scales of a
+    const float* a_shared_scale; // FP8: same for a_shared
+    const void* b;               // [G, N, K]
+    const void* b2;              // [G, N, K] (SwiGLU up) or nullptr
+    const float* b_scale;        // FP8: [G, N/128, K/128]
+    const float* b2_scale;
+    void* out;                   // [*, N] (or [*, N] SwiGLU output)
+    int out_elem;                // Elem of out (kE4M3: out_scale receives [*, N/128])
+    float* out_scale;
+    const float* bias;           // [N] added to the result (router) or nullptr
+    uint32_t* err;
+    int64_t spin_ns;
+};
+
+// Kernel launch accounting (moe_launch_count): every launcher adds the
+// number of kernels it enqueued.
+void count_launches(int n);
+
+// Launchers (all asynchronous on `stream`; return cudaGetLastError()).
+cudaError_t launch_gemm_simt(const GroupedGemm& g, cudaStream_t stream);
+cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t stream);
+bool gemm_tc_supported(const GroupedGemm& g);
+
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* blob, uint32_t* err,
+                        cudaStream_t stream);
+
+cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_t* hist, int32_t* counts,
+                                 int32_t* offsets, int32_t* tiles, int32_t* inv, int32_t* src_tok, uint32_t* err,
+                                 cudaStream_t stream);
+cudaError_t launch_gather_rows(const void* x, int elem_bytes, int64_t row_bytes, const int32_t* src_tok,
+                               int rows, void* xp, cudaStream_t stream);
+cudaError_t launch_quant_rows(const void* x, int x_elem, int rows, int cols, uint8_t* q, float* s,
+                              cudaStream_t stream);
+cudaError_t launch_quant_blocks(const float* w, int64_t groups, int rows, int cols, uint8_t* q, float* s,
+                                cudaStream_t stream);
+cudaError_t launch_unpermute(const void* y, int y_elem, const int32_t* blob, const int32_t* inv, int T, int D,
+                             int k, void* out, int out_elem, uint32_t* err, cudaStream_t stream);
+cudaError_t launch_selftest_timeout(uint32_t* err, int64_t limit_ns, cudaStream_t stream);
+
+}  // namespace moe

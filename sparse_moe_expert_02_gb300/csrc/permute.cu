@@ -1,0 +1,258 @@
+// Expert-contiguous permutation of the routed (token, slot) pairs, row
+// gathers, and the E4M3 quantisers.
+//
+// The grouped layout is what the expert GEMMs stream over; its inverse is
+// the unpermutation of "Systems engineering playbook: Qwen 3.5 MoE on
+// Ironwood TPU" (English page, table in "Pallas Kernels, SparseCore
+// Co-Design, and the Roofline").  The order inside each expert's segment is
+// the row-major (t, j) order of the pairs -- a stable counting sort -- so the
+// layout is deterministic and needs no atomics for positions:
+//   1. hist:   per chunk of kPermChunk pairs, a histogram over experts;
+//   2. scan:   per expert, an exclusive scan over chunks; then counts,
+//              offsets (with the shared expert's T rows appended) and the
+//              prefix of 128-row tiles the GEMMs walk;
+//   3. rank:   per chunk, one warp walks its pairs in order, ranking equal
+//              experts inside each 32-pair step with __match_any_sync, and
+//              writes inv[pair] and src_tok[row].
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ hist
+
+__global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restrict__ idx, int64_t TK, int E,
+                                                        int32_t* __restrict__ hist, uint32_t* err) {
+    extern __shared__ int32_t sh[];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+    __syncthreads();
+    const int64_t a0 = (int64_t)blockIdx.x * kPermChunk;
+    for (int i = threadIdx.x; i < kPermChunk; i += blockDim.x) {
+        int64_t a = a0 + i;
+        if (a < TK) {
+            int e = __ldg(idx + a);
+            if ((unsigned)e < (unsigned)E) atomicAdd(&sh[e], 1);
+            else record_error(err, MOE_ERR_BOUNDS, (uint32_t)a, (uint32_t)e, 1);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = sh[e];
+}
+
+// ------------------------------------------------------------------ scan
+
+// Warp-wide exclusive scan of n <= 32*33 values in smem `v` into `out`
+// (out[n] = total).  Lane l owns a contiguous segment.
+__device__ void warp_exclusive_scan(const int32_t* v, int n, int32_t* out) {
+    const int lane = threadIdx.x & 31;
+    const int seg = (n + 31) / 32;
+    const int b = lane * seg, e = min(n, b + seg);
+    int s = 0;
+    for (int i = b; i < e; ++i) s += v[i];
+    int incl = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    int run = incl - s;
+    for (int i = b; i < e; ++i) { out[i] = run; run += v[i]; }
+    if (lane == 31) out[n] = incl;
+}
+
+__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E, int T,
+                                                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                                                         int32_t* __restrict__ tiles) {
+    __shared__ int32_t cnt[1025 + 1];
+    __shared__ int32_t ntile[1025 + 1];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int c = 0; c < nchunks; ++c) {
+            int64_t i = (int64_t)c * E + e;
+            int v = hist[i];
+            hist[i] = run;
+            run += v;
+        }
+        cnt[e] = run;
+        ntile[e] = (run + kRowTile - 1) / kRowTile;
+    }
+    if (threadIdx.x == 0) {
+        cnt[E] = T;
+        ntile[E] = (T + kRowTile - 1) / kRowTile;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) counts[e] = cnt[e];
+    if (threadIdx.x < 32) warp_exclusive_scan(cnt, E + 1, offsets);
+    else if (threadIdx.x < 64) warp_exclusive_scan(ntile, E + 1, tiles);
+}
+
+// ------------------------------------------------------------------ rank
+
+__global__ void __launch_bounds__(32) perm_rank_kernel(const int32_t* __restrict__ idx, int64_t TK, int k, int E,
+                                                       const int32_t* __restrict__ hist,
+                                                       const int32_t* __restrict__ offsets,
+                                                       int32_t* __restrict__ inv, int32_t* __restrict__ src_tok) {
+    extern __shared__ int32_t cursor[];
+    const int lane = threadIdx.x;
+    const int64_t a0 = (int64_t)blockIdx.x * kPermChunk;
+    for (int e = lane; e < E; e += 32) cursor[e] = __ldg(offsets + e) + __ldg(hist + (int64_t)blockIdx.x * E + e);
+    __syncwarp();
+    const unsigned lt = (1u << lane) - 1u;
+    for (int s = 0; s < kPermChunk; s += 32) {
+        const int64_t a = a0 + s + lane;
+        const bool valid = a < TK;
+        int e = valid ? __ldg(idx + a) : -1;
+        if ((unsigned)e >= (unsigned)E) e = -1;  // out-of-range ids were reported by hist
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        int pos = 0;
+        if (e >= 0) pos = cursor[e] + __popc(peers & lt);
+        __syncwarp();
+        if (e >= 0 && (peers >> lane) == 1u) cursor[e] += __popc(peers);  // highest lane of the group
+        __syncwarp();
+        if (e >= 0) {
+            inv[a] = pos;
+            src_tok[pos] = (int32_t)(a / k);
+        }
+        if (a0 + s + 32 >= TK) break;
+    }
+}
+
+__global__ void shared_rows_kernel(int32_t* __restrict__ src_tok, int64_t TK, int T) {
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) src_tok[TK + t] = t;
+}
+
+cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_t* hist, int32_t* counts,
+                                 int32_t* offsets, int32_t* tiles, int32_t* inv, int32_t* src_tok, uint32_t* err,
+                                 cudaStream_t stream) {
+    const int64_t TK = (int64_t)T * k;
+    const int nch = (int)cdiv(TK, kPermChunk);
+    perm_hist_kernel<<<nch, 256, E * sizeof(int32_t), stream>>>(idx, TK, E, hist, err);
+    perm_scan_kernel<<<1, 1024, 0, stream>>>(hist, nch, E, T, counts, offsets, tiles);
+    perm_rank_kernel<<<nch, 32, E * sizeof(int32_t), stream>>>(idx, TK, k, E, hist, offsets, inv, src_tok);
+    shared_rows_kernel<<<(unsigned)cdiv(T, 256), 256, 0, stream>>>(src_tok, TK, T);
+    count_launches(4);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- gather
+
+// xp[p] = x[src_tok[p]] for p < rows; one warp per row, 16-byte vectors when
+// the row size allows, else 4-byte words.
+template <typename V>
+__global__ void __launch_bounds__(256) gather_rows_kernel(const V* __restrict__ x, int64_t row_vecs,
+                                                          const int32_t* __restrict__ src_tok, int rows,
+                                                          V* __restrict__ xp) {
+    const int lane = threadIdx.x & 31;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
+        const V* src = x + (int64_t)__ldg(src_tok + r) * row_vecs;
+        V* dst = xp + (int64_t)r * row_vecs;
+        for (int64_t i = lane; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
+    }
+}
+
+cudaError_t launch_gather_rows(const void* x, int elem_bytes, int64_t row_bytes, const int32_t* src_tok, int rows,
+                               void* xp, cudaStream_t stream) {
+    (void)elem_bytes;
+    if (rows <= 0) return cudaGetLastError();
+    int blocks = (int)std::min<int64_t>(cdiv(rows, 8), 148 * 16);
+    if (row_bytes % 16 == 0)
+        gather_rows_kernel<int4><<<blocks, 256, 0, stream>>>((const int4*)x, row_bytes / 16, src_tok, rows, (int4*)xp);
+    else
+        gather_rows_kernel<int32_t><<<blocks, 256, 0, stream>>>((const int32_t*)x, row_bytes / 4, src_tok, rows,
+                                                               (int32_t*)xp);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- quantisers
+
+// Per row, per 128-column group: s = amax / 448 (1 if the group is all
+// zero), code = E4M3_rne_satfinite(fp32(v * fp32(448 / amax))).  One warp
+// per group, four columns per lane.
+template <typename T>
+__global__ void __launch_bounds__(256) quant_rows_kernel(const T* __restrict__ x, int rows, int cols,
+                                                         uint8_t* __restrict__ q, float* __restrict__ s) {
+    const int lane = threadIdx.x & 31;
+    const int gpr = cols / 128;
+    const int64_t ngroups = (int64_t)rows * gpr;
+    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; g < ngroups; g += warps) {
+        const int64_t r = g / gpr, c0 = (g % gpr) * 128 + lane * 4;
+        const T* src = x + r * cols + c0;
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = to_f32(src[i]);
+        float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        float sc = __fdiv_rn(amax, 448.0f), inv = __fdiv_rn(448.0f, amax);
+        if (amax == 0.0f) { sc = 1.0f; inv = 1.0f; }
+        uint32_t packed = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) packed |= (uint32_t)f32_to_e4m3(__fmul_rn(v[i], inv)) << (8 * i);
+        *(uint32_t*)(q + r * cols + c0) = packed;
+        if (lane == 0) s[g] = sc;
+    }
+}
+
+cudaError_t launch_quant_rows(const void* x, int x_elem, int rows, int cols, uint8_t* q, float* s,
+                              cudaStream_t stream) {
+    if (rows <= 0) return cudaGetLastError();
+    int64_t groups = (int64_t)rows * (cols / 128);
+    int blocks = (int)std::min<int64_t>(cdiv(groups, 8), 148 * 32);
+    if (x_elem == kBF16)
+        quant_rows_kernel<bf16><<<blocks, 256, 0, stream>>>((const bf16*)x, rows, cols, q, s);
+    else
+        quant_rows_kernel<float><<<blocks, 256, 0, stream>>>((const float*)x, rows, cols, q, s);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// One block per 128x128 weight block of a [groups, rows, cols] fp32 tensor.
+__global__ void __launch_bounds__(256) quant_blocks_kernel(const float* __restrict__ w, int rows, int cols,
+                                                           uint8_t* __restrict__ q, float* __restrict__ s) {
+    __shared__ float red[8];
+    const int nbr = rows / 128, nbc = cols / 128;
+    const int64_t b = blockIdx.x;
+    const int64_t g = b / (nbr * nbc);
+    const int br = (int)((b / nbc) % nbr), bc = (int)(b % nbc);
+    const float* base = w + g * (int64_t)rows * cols + (int64_t)br * 128 * cols + bc * 128;
+    uint8_t* qb = q + g * (int64_t)rows * cols + (int64_t)br * 128 * cols + bc * 128;
+    const int c4 = (threadIdx.x & 31) * 4, r0 = threadIdx.x >> 5;  // 8 rows per pass
+    float amax = 0.0f;
+    for (int r = r0; r < 128; r += 8) {
+        float4 v = *(const float4*)(base + (int64_t)r * cols + c4);
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[i]);
+    float sc = __fdiv_rn(amax, 448.0f), inv = __fdiv_rn(448.0f, amax);
+    if (amax == 0.0f) { sc = 1.0f; inv = 1.0f; }
+    if (threadIdx.x == 0) s[b] = sc;
+    for (int r = r0; r < 128; r += 8) {
+        float4 v = *(const float4*)(base + (int64_t)r * cols + c4);
+        uint32_t packed = (uint32_t)f32_to_e4m3(__fmul_rn(v.x, inv)) | ((uint32_t)f32_to_e4m3(__fmul_rn(v.y, inv)) << 8) |
+                          ((uint32_t)f32_to_e4m3(__fmul_rn(v.z, inv)) << 16) |
+                          ((uint32_t)f32_to_e4m3(__fmul_rn(v.w, inv)) << 24);
+        *(uint32_t*)(qb + (int64_t)r * cols + c4) = packed;
+    }
+}
+
+cudaError_t launch_quant_blocks(const float* w, int64_t groups, int rows, int cols, uint8_t* q, float* s,
+                                cudaStream_t stream) {
+    int64_t nb = groups * (rows / 128) * (cols / 128);
+    if (nb <= 0) return cudaGetLastError();
+    quant_blocks_kernel<<<(unsigned)nb, 256, 0, stream>>>(w, rows, cols, q, s);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,119 @@
+// Unpermutation with the local reduction and the shared-expert add:
+//   out[t] = y[T*k + t] + sum_j w[t,j] * y[inv[t*k + j]]
+// ("Systems engineering playbook: Qwen 3.5 MoE on Ironwood TPU", English
+// page, table in "Pallas Kernels, SparseCore Co-Design, and the Roofline":
+// token unpermutation plus local reduction offloaded to SparseCore; the
+// shared expert is the always-on path of the MoE bullet in "The
+// Architectural Constraints That Break Naive Sharding").
+//
+// A gather-reduce: one block per token, each thread owns 16-byte vectors of
+// the row, reads the k+1 source rows and accumulates in fp32 in slot order.
+// The routing weights come from plane 1 of the blob.
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+template <typename TY, typename TO>
+__global__ void __launch_bounds__(256) unpermute_kernel(const TY* __restrict__ y, const int32_t* __restrict__ blob,
+                                                        const int32_t* __restrict__ inv, int T, int D, int k,
+                                                        TO* __restrict__ out, uint32_t* err) {
+    constexpr int V = 16 / sizeof(TY);  // elements per 16-byte vector of y
+    __shared__ int64_t rows[33];
+    __shared__ float wts[32];
+    const int t = blockIdx.x;
+    const int64_t TK = (int64_t)T * k;
+    if (threadIdx.x < k) {
+        int r = __ldg(inv + (int64_t)t * k + threadIdx.x);
+        float wj = __int_as_float(__ldg(blob + TK + (int64_t)t * k + threadIdx.x));
+        if ((unsigned)r >= (unsigned)TK) {  // a pair the permutation dropped (bad expert id)
+            record_error(err, MOE_ERR_BOUNDS, (uint32_t)t, (uint32_t)threadIdx.x, 2);
+            r = 0;
+            wj = 0.0f;
+        }
+        rows[threadIdx.x] = (int64_t)r * D;
+        wts[threadIdx.x] = wj;
+    }
+    if (threadIdx.x == 0) rows[32] = (TK + t) * D;
+    __syncthreads();
+    for (int c = threadIdx.x * V; c < D; c += blockDim.x * V) {
+        float acc[V];
+        {
+            const int4 v = __ldg((const int4*)(y + rows[32] + c));
+            const TY* e = (const TY*)&v;
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] = to_f32(e[i]);
+        }
+        for (int j = 0; j < k; ++j) {
+            const int4 v = __ldg((const int4*)(y + rows[j] + c));
+            const TY* e = (const TY*)&v;
+            const float wj = wts[j];
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] = fmaf(wj, to_f32(e[i]), acc[i]);
+        }
+        TO* o = out + (int64_t)t * D + c;
+        if constexpr (sizeof(TO) == 4) {
+#pragma unroll
+            for (int i = 0; i < V; i += 4) *(float4*)(o + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+        } else {
+#pragma unroll
+            for (int i = 0; i < V; i += 8) {
+                uint4 p;
+                __nv_bfloat162* pb = (__nv_bfloat162*)&p;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) pb[q] = __floats2bfloat162_rn(acc[i + 2 * q], acc[i + 2 * q + 1]);
+                *(uint4*)(o + i) = p;
+            }
+        }
+    }
+}
+
+cudaError_t launch_unpermute(const void* y, int y_elem, const int32_t* blob, const int32_t* inv, int T, int D, int k,
+                             void* out, int out_elem, uint32_t* err, cudaStream_t stream) {
+    if (T <= 0) return cudaGetLastError();
+    const int V = (y_elem == kF32) ? 4 : 8;
+    int threads = (int)std::min<int64_t>(256, ((D / V + 31) / 32) * 32);
+    if (y_elem == kF32 && out_elem == kF32)
+        unpermute_kernel<float, float><<<T, threads, 0, stream>>>((const float*)y, blob, inv, T, D, k, (float*)out, err);
+    else if (y_elem == kF32)
+        unpermute_kernel<float, bf16><<<T, threads, 0, stream>>>((const float*)y, blob, inv, T, D, k, (bf16*)out, err);
+    else if (out_elem == kF32)
+        unpermute_kernel<bf16, float><<<T, threads, 0, stream>>>((const bf16*)y, blob, inv, T, D, k, (float*)out, err);
+    else
+        unpermute_kernel<bf16, bf16><<<T, threads, 0, stream>>>((const bf16*)y, blob, inv, T, D, k, (bf16*)out, err);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+// Bounded-wait self-test: one thread waits on an mbarrier that expects an
+// arrival nobody makes, polling %globaltimer, and gives up after limit_ns.
+__global__ void selftest_timeout_kernel(uint32_t* err, int64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(&bar);
+    if (threadIdx.x == 0) asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(1));
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        uint32_t done = 0;
+        while (!done) {
+            asm volatile(
+                "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+                : "=r"(done)
+                : "r"(a), "r"(0));
+            if (!done && (int64_t)(globaltimer_ns() - t0) > limit_ns) {
+                record_error(err, MOE_ERR_DEVICE_TIMEOUT, 0xFFFFu, 0, 0);
+                break;
+            }
+        }
+    }
+}
+
+cudaError_t launch_selftest_timeout(uint32_t* err, int64_t limit_ns, cudaStream_t stream) {
+    selftest_timeout_kernel<<<1, 32, 0, stream>>>(err, limit_ns);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,271 @@
+"""Parity of the CUDA path (through the C ABI) against the fp64 oracle.
+
+Integer and index work (top-k indices, counts, offsets, tiles, inverse
+permutation, source tokens, gathered rows) must match bit for bit when both
+sides start from the same fp32 router logits.  Floating-point outputs must
+satisfy max|err| <= 1e-2 * rms(out) (bf16 and fp32 layers) and
+<= 5e-2 * rms(out) (FP8 layer), the tolerances the layer is specified with.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from parity_util import err_quantiles, experts_for_tokens, rel_max_err, sample_rows
+from sparse_moe_expert_02_gb300 import MoELayer, synth
+from sparse_moe_expert_02_gb300 import _lib as L
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-2, "bf16": 1e-2, "fp8": 5e-2}
+
+
+def _dev_inputs(shape, seed=0, weights=True):
+    return synth.make_inputs(shape, seed=seed, device="cuda", weights=weights)
+
+
+def _routing_parity(layer, T, E, k):
+    """Bit-exact routing and permutation given the GPU's fp32 logits."""
+    v = layer.views(T)
+    logits = v["logits"].double().cpu().numpy()
+    blob = v["blob"].cpu().numpy()
+    idx_o, w_o = oracle.topk(logits, k)
+    assert np.array_equal(blob[0], idx_o), "top-k indices differ from the oracle on the same logits"
+    w_gpu = blob[1].view(np.float32).astype(np.float64)
+    assert np.allclose(w_gpu, w_o, rtol=1e-6, atol=1e-7)
+    counts, offsets, inv, src = oracle.permute(idx_o, E)
+    assert np.array_equal(v["counts"].cpu().numpy(), counts)
+    assert np.array_equal(v["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(v["inv"].cpu().numpy(), inv)
+    assert np.array_equal(v["src_tok"].cpu().numpy(), src)
+    tiles = np.concatenate([[0], np.cumsum((counts.astype(np.int64) + 127) // 128)])
+    assert np.array_equal(v["tiles"].cpu().numpy(), tiles)
+    return idx_o, w_o, inv, src
+
+
+def _layer_parity(shape, inp, rows=None, flags=0, out_dtype="f32", check_y=True):
+    T, E, k = shape.T, shape.E, shape.top_k
+    layer = MoELayer.from_shape(shape, inp, flags=flags, out_dtype=out_dtype)
+    x = inp["x"]
+    out = layer.forward(x)
+    layer.check()
+    torch.cuda.synchronize()
+    idx, w, inv, src = _routing_parity(layer, T, E, k)
+    v = layer.views(T)
+    if shape.dtype == "fp8":
+        xq = v["xq"]
+        assert torch.equal(v["xp"], xq[torch.as_tensor(src[:T * k], device="cuda").long()])
+    else:
+        assert torch.equal(v["xp"], x[torch.as_tensor(src[:T * k], device="cuda").long()])
+    rows = np.arange(T) if rows is None else rows
+    # router logits against fp64 logits of the same inputs
+    z_ref = oracle.logits(x[rows].cpu(), inp["w_router"].cpu(), inp["b_router"].cpu() if shape.has_bias else None)
+    z_gpu = v["logits"][torch.as_tensor(rows, device="cuda")].double().cpu().numpy()
+    assert np.abs(z_gpu - z_ref).max() <= 2e-4 * max(1.0, np.abs(z_ref).max())
+    # layer output on the sampled rows, oracle routed by the GPU logits
+    ex, idx_sub = experts_for_tokens(idx[rows], layer.w, shape.dtype, E)
+    ref, y_ref = oracle.moe_tokens(x[rows].cpu(), idx_sub, w[rows], ex, want_y=True)
+    got = out[torch.as_tensor(rows, device="cuda")].double().cpu().numpy()
+    err = rel_max_err(got, ref)
+    print(f"{shape.name}: out max|err|/rms = {err:.3e}, quantiles {err_quantiles(got, ref)}")
+    assert err <= TOL[shape.dtype]
+    if check_y:
+        # expert outputs of the grouped layout, slot by slot
+        y = v["y"].double().cpu().numpy()
+        for n, t in enumerate(rows):
+            for j in range(k):
+                r = inv[t * k + j]
+                assert rel_max_err(y[r], y_ref[n, j]) <= 2 * TOL[shape.dtype]
+            assert rel_max_err(y[T * k + t], y_ref[n, k]) <= 2 * TOL[shape.dtype]
+    return layer, out, err
+
+
+# ------------------------------------------------------------- small shapes
+
+def test_tiny_fp32_layer_all_tokens():
+    shape = synth.TINY_F32
+    inp = _dev_inputs(shape, seed=0)
+    _, _, err = _layer_parity(shape, inp)
+    assert err <= 1e-4, "fp32 layer should sit far inside the tolerance"
+
+
+@pytest.mark.parametrize("T", [77, 1, 129])
+def test_small_fp32_ragged(T):
+    shape = synth.SMALL_F32.with_tokens(T)
+    _layer_parity(shape, _dev_inputs(shape, seed=3))
+
+
+@pytest.mark.parametrize("flags", [0, L.MOE_FLAG_FORCE_SIMT], ids=["default", "simt"])
+@pytest.mark.parametrize("T", [300, 1, 128, 129])
+def test_small_bf16_layer(flags, T):
+    shape = synth.SMALL_BF16.with_tokens(T)
+    _layer_parity(shape, _dev_inputs(shape, seed=4), flags=flags)
+
+
+def test_small_bf16_bf16_output():
+    shape = synth.SMALL_BF16
+    inp = _dev_inputs(shape, seed=5)
+    layer32 = MoELayer.from_shape(shape, inp)
+    layer16 = MoELayer.from_shape(shape, inp, out_dtype="bf16")
+    o32 = layer32.forward(inp["x"])
+    o16 = layer16.forward(inp["x"])
+    torch.cuda.synchronize()
+    assert o16.dtype == torch.bfloat16
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+
+
+def test_forward_outputs_blob_and_logits():
+    shape = synth.SMALL_BF16
+    inp = _dev_inputs(shape, seed=6)
+    layer = MoELayer.from_shape(shape, inp)
+    T, k, E = shape.T, shape.top_k, shape.E
+    blob = torch.empty((2, T, k), dtype=torch.int32, device="cuda")
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    layer.forward(inp["x"], blob_out=blob, logits_out=logits)
+    torch.cuda.synchronize()
+    v = layer.views(T)
+    assert torch.equal(blob, v["blob"]) and torch.equal(logits, v["logits"])
+    idx, w = oracle.topk(logits.double().cpu().numpy(), k)
+    assert np.array_equal(blob[0].cpu().numpy(), idx)
+
+
+# ------------------------------------------------------------- stage tests
+
+@pytest.mark.parametrize("T,E,k", [(300, 16, 2), (1000, 512, 10), (37, 1000, 32), (5, 7, 7)])
+def test_topk_with_planted_ties(T, E, k):
+    shape = synth.LayerShape("ties", T, 128, E, 128, k, "bf16")
+    layer = MoELayer(shape.D, E, shape.I, k, "bf16", {"w_router": None, "w_gate": None, "w_up": None,
+                                                      "w_down": None}, T)
+    z = synth.tie_logits(T, E, seed=T + k, device="cuda")
+    v = layer.views(T)
+    v["logits"].copy_(z)
+    layer.topk(T)
+    torch.cuda.synchronize()
+    idx, w = oracle.topk(z.double().cpu().numpy(), k)
+    blob = v["blob"].cpu().numpy()
+    assert np.array_equal(blob[0], idx)
+    assert np.allclose(blob[1].view(np.float32), w, rtol=1e-6, atol=1e-7)
+    layer.check()
+
+
+@pytest.mark.parametrize("T,E,k,s", [(3000, 512, 10, 1.2), (1, 512, 10, 1.0), (2049, 64, 4, 2.0)])
+def test_permute_given_indices(T, E, k, s):
+    """Routing fed in directly: a skewed draw with many pairs per chunk."""
+    D = 256
+    layer = MoELayer(D, E, 128, k, "bf16", {"w_router": None, "w_gate": None, "w_up": None, "w_down": None}, T)
+    g = np.random.default_rng(T)
+    bias = -s * np.log(np.arange(1, E + 1))[g.permutation(E)]
+    z = g.normal(size=(T, E)) + bias
+    idx, w = oracle.topk(z, k)
+    v = layer.views(T)
+    v["blob"][0].copy_(torch.from_numpy(idx))
+    v["blob"][1].copy_(torch.from_numpy(w.astype(np.float32).view(np.int32)))
+    x = torch.randn((T, D), device="cuda").to(torch.bfloat16)
+    layer.permute(x)
+    torch.cuda.synchronize()
+    counts, offsets, inv, src = oracle.permute(idx, E)
+    assert np.array_equal(v["counts"].cpu().numpy(), counts)
+    assert np.array_equal(v["offsets"].cpu().numpy(), offsets)
+    assert np.array_equal(v["inv"].cpu().numpy(), inv)
+    assert np.array_equal(v["src_tok"].cpu().numpy(), src)
+    assert torch.equal(v["xp"], x[torch.as_tensor(src[:T * k], device="cuda").long()])
+    layer.check()
+
+
+def test_identity_experts_unpermute_round_trip():
+    """y rows := x rows of their source token, shared rows := 0: the combine
+    returns x up to fp32 rounding of sum_j w_j * x (weights sum to one)."""
+    T, E, k, D = 500, 64, 8, 256
+    layer = MoELayer(D, E, 128, k, "f32", {"w_router": None, "w_gate": None, "w_up": None, "w_down": None}, T)
+    g = np.random.default_rng(1)
+    idx, w = oracle.topk(g.normal(size=(T, E)), k)
+    v = layer.views(T)
+    v["blob"][0].copy_(torch.from_numpy(idx))
+    v["blob"][1].copy_(torch.from_numpy(w.astype(np.float32).view(np.int32)))
+    x = torch.randn((T, D), device="cuda")
+    layer.permute(x)
+    src = v["src_tok"].long()
+    v["y"][:T * k].copy_(x[src[:T * k]])
+    v["y"][T * k:].zero_()
+    out = layer.unpermute(T)
+    torch.cuda.synchronize()
+    assert torch.allclose(out, x, rtol=0, atol=8 * k * 2.0 ** -24 * float(x.abs().max()))
+
+
+def test_quantize_weights_bit_exact_with_oracle():
+    g = torch.Generator(device="cuda").manual_seed(0)
+    w = torch.randn((3, 256, 384), generator=g, device="cuda")
+    w[0, :128, :128] *= 1e-3
+    w[1, 128:, 128:256] = 0
+    layer = MoELayer(512, 4, 128, 2, "bf16", {"w_router": None, "w_gate": None, "w_up": None, "w_down": None}, 4)
+    q = torch.empty(w.shape, dtype=torch.uint8, device="cuda")
+    s = torch.empty((3, 2, 3), dtype=torch.float32, device="cuda")
+    L.moe_quantize_weights(layer.plan, w, q, s)
+    torch.cuda.synchronize()
+    q_o, s_o = oracle.quant_blocks(w.cpu().numpy(), 128, 128)
+    assert np.array_equal(q.cpu().numpy(), q_o)
+    assert np.array_equal(s.cpu().numpy(), s_o)
+
+
+# ------------------------------------------------------ faults and checks
+
+def test_bounded_wait_times_out_and_reports():
+    layer = MoELayer(128, 4, 128, 2, "bf16", {"w_router": None, "w_gate": None, "w_up": None, "w_down": None}, 4)
+    layer.init_ws()
+    L.moe_selftest_wait_timeout(layer.plan, layer.ws, 2_000_000)   # 2 ms
+    assert L.moe_check_status(layer.plan, layer.ws) == L.MOE_ERR_DEVICE_TIMEOUT
+    layer.init_ws()
+    assert L.moe_check_status(layer.plan, layer.ws) == L.MOE_OK
+    # the context is still usable
+    torch.cuda.synchronize()
+    assert float(torch.ones(4, device="cuda").sum()) == 4.0
+
+
+def test_nonfinite_logit_is_reported():
+    shape = synth.SMALL_BF16.with_tokens(40)
+    inp = _dev_inputs(shape, seed=7)
+    inp["x"][5, 3] = float("nan")
+    layer = MoELayer.from_shape(shape, inp)
+    layer.forward(inp["x"])
+    assert L.moe_check_status(layer.plan, layer.ws) == L.MOE_ERR_NONFINITE
+
+
+def test_host_argument_errors():
+    shape = synth.SMALL_BF16.with_tokens(64)
+    inp = _dev_inputs(shape, seed=8)
+    layer = MoELayer.from_shape(shape, inp)
+    x = inp["x"]
+    with pytest.raises(L.MoEError) as e:
+        big = torch.cat([x, x])
+        layer.forward(big)                               # T > T_max
+    assert e.value.status == L.MOE_ERR_INVALID_ARG
+    with pytest.raises(L.MoEError) as e:                 # misaligned x
+        xs = torch.empty(x.numel() + 8, dtype=x.dtype, device="cuda")[1:1 + x.numel()].view(x.shape)
+        L.moe_forward(layer.plan, layer.cw, xs, 64, layer.new_out(64), None, None, layer.ws)
+    assert e.value.status == L.MOE_ERR_INVALID_ARG
+    with pytest.raises(L.MoEError) as e:                 # workspace too small
+        L.moe_forward(layer.plan, layer.cw, x, 64, layer.new_out(64), None, None, layer.ws[:4096])
+    assert e.value.status == L.MOE_ERR_WORKSPACE
+
+
+# ------------------------------------------------------ full-size workloads
+
+@pytest.fixture(scope="module")
+def big_bf16_weights():
+    w = synth.make_inputs(synth.DECODE_BF16, seed=0, device="cuda", T=1)
+    yield {n: w[n] for n in ("w_gate", "w_up", "w_down")}
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("shape", [synth.DECODE_BF16, synth.BATCHED_DECODE_BF16, synth.PREFILL_BF16],
+                         ids=lambda s: s.name)
+def test_full_size_bf16_workloads(shape, big_bf16_weights):
+    inp = _dev_inputs(shape, seed=0, weights=False)
+    inp.update(big_bf16_weights)
+    rows = sample_rows(shape.T, 6, seed=1)
+    layer, out, _ = _layer_parity(shape, inp, rows=rows, check_y=False)
+    if shape.zipf_s is not None and shape.T >= 8192:
+        counts = layer.views(shape.T)["counts"][:shape.E].cpu().numpy()
+        mean = shape.T * shape.top_k / shape.E
+        assert counts.max() > 10 * mean, "the skewed workload must have straggler experts"
+    assert torch.isfinite(out).all()
