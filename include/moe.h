@@ -78,8 +78,9 @@ typedef enum moe_status {
 /* Arithmetic type of the layer.
  *   MOE_F32: fp32 activations and weights, fp32 arithmetic throughout (no
  *     tensor cores).
- *   MOE_BF16: bf16 x, weights and intermediates (permuted x, h, expert
- *     outputs), fp32 accumulation, fp32 or bf16 output.
+ *   MOE_BF16: bf16 x and weights, fp32 accumulation; the permuted x is bf16,
+ *     h is kept as a bf16 hi/lo pair and the expert outputs in fp32, so the
+ *     layer stays within 1e-2 of the output rms; fp32 or bf16 output.
  *   MOE_FP8_E4M3_B128: expert weights as E4M3 codes with one fp32 scale per
  *     128x128 block; both expert GEMM inputs (x and h) quantised to E4M3 per
  *     token per 128-column group with s = amax/448 and
@@ -133,9 +134,11 @@ typedef struct moe_ws_layout {
     size_t xq_scale;   /* FP8: f32 [T, D/128] */
     size_t xp;         /* [T*top_k, D] x gathered into grouped order (layer dtype; E4M3 for FP8) */
     size_t xp_scale;   /* FP8: f32 [T*top_k, D/128] */
-    size_t h;          /* [T*top_k + T, I] SwiGLU activations (f32 | bf16 | E4M3) */
+    size_t h;          /* SwiGLU activations: f32 [R, I] | bf16 hi/lo pair [R, 2I] (hi in
+                          columns 0..I-1, lo = bf16(h - hi) in I..2I-1) | E4M3 [R, I];
+                          R = T*top_k + T */
     size_t h_scale;    /* FP8: f32 [T*top_k + T, I/128] */
-    size_t y;          /* [T*top_k + T, D] expert outputs (f32 for MOE_F32, else bf16) */
+    size_t y;          /* [R, D] expert outputs: f32 (MOE_F32, MOE_BF16) or bf16 (FP8 layer) */
 } moe_ws_layout;
 
 /* Validate a configuration and build a host-side plan for `device`.

@@ -68,9 +68,14 @@ void layout(const moe_config& c, int T, moe_ws_layout* L) {
     L->xq_scale = fp8 ? take((size_t)T * (c.D / 128) * 4) : 0;
     L->xp = take((size_t)TK * c.D * ab);
     L->xp_scale = fp8 ? take((size_t)TK * (c.D / 128) * 4) : 0;
-    L->h = take((size_t)R * c.I * ab);
+    // bf16 layer: h is a bf16 hi/lo pair per element ([R, 2I]); the pair
+    // keeps the down GEMM's input at ~fp32 precision (a single bf16 rounding
+    // of h alone costs about 1e-2 of the output rms).
+    L->h = take((size_t)R * c.I * (c.dtype == MOE_BF16 ? 4 : ab));
     L->h_scale = fp8 ? take((size_t)R * (c.I / 128) * 4) : 0;
-    L->y = take((size_t)R * c.D * (c.dtype == MOE_F32 ? 4 : 2));
+    // y in fp32 except for the FP8 layer (bf16 there): a bf16 y alone costs
+    // about 1.3e-2 of the output rms, above the bf16 layer's tolerance.
+    L->y = take((size_t)R * c.D * (c.dtype == MOE_FP8_E4M3_B128 ? 2 : 4));
     L->total = o;
 }
 
@@ -245,7 +250,9 @@ moe_status moe_route(const moe_plan* p, const moe_weights* w, const void* x, int
     g.rows = T;
     g.max_tiles = (int)moe::cdiv(T, moe::kRowTile);
     g.N = c.E;
-    g.K = c.D;
+    g.Ka = g.Kb = c.D;
+    g.ldo = c.E;
+    g.a_rows = T;
     g.elem = in_elem(c.dtype);
     g.a = x;
     g.b = w->w_router;
@@ -300,7 +307,11 @@ moe_status moe_gemm_gateup(const moe_plan* p, const moe_weights* w, const void* 
     g.tiles = W.at<int32_t>(W.L.tiles);
     g.max_tiles = grouped_max_tiles(c, T);
     g.N = c.I;
-    g.K = c.D;
+    g.Ka = g.Kb = c.D;
+    g.out_pair = c.dtype == MOE_BF16;
+    g.ldo = g.out_pair ? 2 * c.I : c.I;
+    g.a_rows = T * c.top_k;
+    g.a_shared_rows = T;
     g.elem = act_elem(c.dtype);
     g.a = W.at<void>(W.L.xp);
     g.a_shared = fp8 ? (const void*)W.at<uint8_t>(W.L.xq) : x;
@@ -333,14 +344,17 @@ moe_status moe_gemm_down(const moe_plan* p, const moe_weights* w, int32_t T, voi
     g.tiles = W.at<int32_t>(W.L.tiles);
     g.max_tiles = grouped_max_tiles(c, T);
     g.N = c.D;
-    g.K = c.I;
+    g.Kb = c.I;
+    g.Ka = (c.dtype == MOE_BF16) ? 2 * c.I : c.I;  // hi/lo pair walks W_down twice
+    g.ldo = c.D;
+    g.a_rows = T * (c.top_k + 1);
     g.elem = act_elem(c.dtype);
     g.a = W.at<void>(W.L.h);
     g.a_scale = fp8 ? W.at<float>(W.L.h_scale) : nullptr;
     g.b = w->w_down;
     g.b_scale = w->s_down;
     g.out = W.at<void>(W.L.y);
-    g.out_elem = (c.dtype == MOE_F32) ? moe::kF32 : moe::kBF16;
+    g.out_elem = fp8 ? moe::kBF16 : moe::kF32;
     g.err = W.at<uint32_t>(W.L.err);
     g.spin_ns = p->spin_ns;
     return run_gemm(p, g, (cudaStream_t)stream, "down GEMM");
@@ -352,7 +366,7 @@ moe_status moe_unpermute(const moe_plan* p, int32_t T, void* out, void* ws, size
     if (st != MOE_OK) return st;
     if (!ptr_ok(out)) return arg_fail(MOE_ERR_INVALID_ARG, "out NULL or misaligned");
     const moe_config& c = p->cfg;
-    MOE_CUDA(moe::launch_unpermute(W.at<void>(W.L.y), c.dtype == MOE_F32 ? moe::kF32 : moe::kBF16,
+    MOE_CUDA(moe::launch_unpermute(W.at<void>(W.L.y), c.dtype == MOE_FP8_E4M3_B128 ? moe::kBF16 : moe::kF32,
                                    W.at<int32_t>(W.L.blob), W.at<int32_t>(W.L.inv), T, c.D, c.top_k, out,
                                    c.out_dtype == MOE_F32 ? moe::kF32 : moe::kBF16, W.at<uint32_t>(W.L.err),
                                    (cudaStream_t)stream));

@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GroupedGemm g) {
     __shared__ float Bs[BK][BN + 4];
     __shared__ float Bs2[SWIGLU ? BK : 1][BN + 4];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    const int N = g.N, K = g.K;
+    const int N = g.N, Ka = g.Ka, Kb = g.Kb;
     const int n0 = blockIdx.y * BN;
     const int total = g.offsets ? __ldg(g.tiles + g.G) : (int)cdiv(g.rows, BM);
     const TE* A = (const TE*)g.a;
@@ -57,9 +57,9 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GroupedGemm g) {
             out0 = 0;
             nrows = g.rows;
         }
-        const TE* abase = (grp == g.shared_group) ? As_ : A + (int64_t)out0 * K;
-        const TE* b1 = (const TE*)g.b + (int64_t)grp * N * K;
-        const TE* b2 = SWIGLU ? (const TE*)g.b2 + (int64_t)grp * N * K : nullptr;
+        const TE* abase = (grp == g.shared_group) ? As_ : A + (int64_t)out0 * Ka;
+        const TE* b1 = (const TE*)g.b + (int64_t)grp * N * Kb;
+        const TE* b2 = SWIGLU ? (const TE*)g.b2 + (int64_t)grp * N * Kb : nullptr;
         float acc[8][4], acc2[SWIGLU ? 8 : 1][4];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -70,16 +70,17 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GroupedGemm g) {
         const int br = tid >> 2, bk = (tid & 3) * 4;   // B: 64 rows x 16 k
         const bool a_ok = (m0 + ar) < nrows;
         const bool b_ok = (n0 + br) < N;
-        for (int k0 = 0; k0 < K; k0 += BK) {
+        for (int k0 = 0; k0 < Ka; k0 += BK) {
             float av[8], bv[4], bv2[4];
-            if (a_ok) load8<TE>(abase + (int64_t)(m0 + ar) * K + k0 + ak, av);
+            const int kb0 = k0 % Kb;  // a hi/lo pair of A walks B twice
+            if (a_ok) load8<TE>(abase + (int64_t)(m0 + ar) * Ka + k0 + ak, av);
             else {
 #pragma unroll
                 for (int i = 0; i < 8; ++i) av[i] = 0.f;
             }
             if (b_ok) {
-                load4<TE>(b1 + (int64_t)(n0 + br) * K + k0 + bk, bv);
-                if (SWIGLU) load4<TE>(b2 + (int64_t)(n0 + br) * K + k0 + bk, bv2);
+                load4<TE>(b1 + (int64_t)(n0 + br) * Kb + kb0 + bk, bv);
+                if (SWIGLU) load4<TE>(b2 + (int64_t)(n0 + br) * Kb + kb0 + bk, bv2);
             } else {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) { bv[i] = 0.f; bv2[i] = 0.f; }
@@ -123,7 +124,10 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GroupedGemm g) {
                 if (n >= N) continue;
                 float v = SWIGLU ? swiglu(acc[i][j], acc2[i][j]) : acc[i][j];
                 if (g.bias) v += __ldg(g.bias + n);
-                out[(int64_t)(out0 + m) * N + n] = from_f32<TO>(v);
+                const int64_t o = (int64_t)(out0 + m) * g.ldo + n;
+                const TO hi = from_f32<TO>(v);
+                out[o] = hi;
+                if (g.out_pair) out[o + N] = from_f32<TO>(v - to_f32(hi));
             }
         }
         __syncthreads();

@@ -1,8 +1,553 @@
-// Tensor-core grouped GEMM (placeholder until the tcgen05 kernel lands).
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMA + TMEM).
+//
+// The expert FFNs of the routed-MoE layer are "Grouped GEMMs" in the sense of
+// "Systems engineering playbook: Qwen 3.5 MoE on Ironwood TPU" (English page,
+// intro and "Pallas Kernels, SparseCore Co-Design, and the Roofline"): one
+// GEMM per expert over that expert's rows of the grouped layout.  Here one
+// persistent kernel walks all of them.
+//
+// Work unit: 128 rows of one group (M, the TMEM lanes) x one block of output
+// features (N <= 256, the TMEM columns).  Units are numbered row-tile major,
+// feature block minor, so the CTAs that run at the same time share a row tile
+// (A read once) and the row tiles of a group run back to back (its weight
+// block is reused from L2).  The row tiles come from the device-built prefix
+// of ceil(rows/128) per group; no host round trip.
+//
+// Warp roles (192 threads, one CTA per SM):
+//   warp 0      TMA producer: A rows (16-row boxes, only the boxes that hold
+//               valid rows) and the B weight tile into a 4-stage ring;
+//   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16,
+//               M=128, N=BN, K=16, fp32 accumulation in TMEM;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (two TMEM buffers,
+//               so the epilogue of one unit overlaps the MMAs of the next),
+//               SwiGLU / bias / conversion, stores.
+// Operands are K-major with the 128-byte swizzle on both sides (TMA writes
+// it, the UMMA descriptor reads it).  Every mbarrier wait is bounded by
+// spin_ns; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its
+// own copies and MMAs (again bounded), frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
-bool gemm_tc_supported(const GroupedGemm&) { return false; }
-cudaError_t launch_gemm_tc(const GroupedGemm&, int, cudaStream_t) { return cudaErrorNotSupported; }
+namespace tc {
+
+constexpr int BM = 128;                   // rows per unit (TMEM lanes)
+constexpr int BK = 64;                    // K per stage: 64 bf16 = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BK * 2;      // 16 KB
+constexpr int kBBytesMax = 256 * BK * 2;  // 32 KB
+constexpr int kThreads = 192;
+constexpr int kAccCols = 256;             // TMEM columns per accumulator buffer
+constexpr int kBoxRowsA = 16;             // A is fetched in 16-row boxes (2 KB)
+constexpr uint32_t kSmemBytes = 1024 + kStages * (kABytes + kBBytesMax) + 256;
+
+enum Epi : int { EPI_SWIGLU = 0, EPI_PLAIN = 1 };
+
+struct Params {
+    int G, shared_group;
+    const int32_t* offsets;
+    const int32_t* tiles;
+    int rows;            // single-group row count (offsets == nullptr)
+    int NB;              // feature blocks per row tile
+    int BN;              // MMA N (SwiGLU: 128 gate + 128 up)
+    int N;               // output features of a group
+    int KB;              // k-blocks walked over A (Ka / 64)
+    int KBb;             // k-blocks of B (Kb / 64); B's k-block is kb % KBb
+    int b_group_rows;    // rows of B per group
+    int ldo;
+    int out_pair;
+    int out_f32;
+    void* out;
+    const float* bias;
+    uint32_t* err;
+    int64_t spin_ns;
+};
+
+// ----------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait for the phase of parity `parity`; false on timeout or abort.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int64_t limit_ns, volatile int* abort) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try(bar, parity)) return true;
+        if (*abort) return false;
+        if ((int64_t)(globaltimer_ns() - t0) > limit_ns) return false;
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows
+// of 128 bytes, 8-row groups 1024 bytes apart (SBO).  LBO is unused by the
+// swizzled K-major layout (set to 1).  Bits 46-47: descriptor version 1.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i gets lane (base+i).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ------------------------------------------------------------ unit decode
+
+struct Unit {
+    int g, m0, row0, nrows, nb;
+};
+
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+    Unit r;
+    const int rt = u / p.NB;
+    r.nb = u - rt * p.NB;
+    if (p.offsets) {
+        r.g = find_group(p.tiles, p.G, rt);
+        r.m0 = (rt - __ldg(p.tiles + r.g)) * BM;
+        r.row0 = __ldg(p.offsets + r.g);
+        r.nrows = __ldg(p.offsets + r.g + 1) - r.row0;
+    } else {
+        r.g = 0;
+        r.m0 = rt * BM;
+        r.row0 = 0;
+        r.nrows = p.rows;
+    }
+    return r;
+}
+
+__device__ __forceinline__ void store_bf16x32(bf16* dst, const float* v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 pk;
+        __nv_bfloat162* h2 = (__nv_bfloat162*)&pk;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+        *(uint4*)(dst + 8 * q) = pk;
+    }
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_sh,
+                   const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
+                   const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kStages * kABytes;
+    uint64_t* bars = (uint64_t*)(sB + kStages * kBBytesMax);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+    const uint32_t tfull0 = smem_u32(bars + 2 * kStages), tempty0 = smem_u32(bars + 2 * kStages + 2);
+    const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
+    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kStages + 5);
+    volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull0 + 8 * b, 1);
+            mbar_init(tempty0 + 8 * b, 4);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(2 * kAccCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int total_tiles = p.offsets ? __ldg(p.tiles + p.G) : (p.rows + BM - 1) / BM;
+    const int total_units = total_tiles * p.NB;
+    const int64_t lim = p.spin_ns;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            int stage = 0;
+            uint32_t phase = 0, armed = 0, armed_parity = 0;
+            const uint32_t b_bytes = (EPI == EPI_SWIGLU) ? 2u * 128 * BK * 2 : (uint32_t)p.BN * BK * 2;
+            bool ok = true;
+            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+                const Unit un = decode_unit(p, u);
+                const bool sh = un.g == p.shared_group;
+                const CUtensorMap* ta = sh ? &tm_a_sh : &tm_a;
+                const int a_y = sh ? un.m0 : un.row0 + un.m0;
+                const int valid = min(BM, un.nrows - un.m0);
+                const int nbox = (valid + kBoxRowsA - 1) / kBoxRowsA;
+                const uint32_t bytes = (uint32_t)nbox * kBoxRowsA * BK * 2 + b_bytes;
+                const int b_y = un.g * p.b_group_rows + un.nb * ((EPI == EPI_SWIGLU) ? 128 : p.BN);
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, lim, abort_flag)) {
+                        record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 1, blockIdx.x, u);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full0 + 8 * stage;
+                    mbar_expect_tx(fb, bytes);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    const uint32_t a_dst = smem_u32(sA + stage * kABytes);
+                    const uint32_t b_dst = smem_u32(sB + stage * kBBytesMax);
+                    for (int i = 0; i < nbox; ++i) tma_load_2d(a_dst + i * kBoxRowsA * 128, ta, fb, kb * BK, a_y + i * kBoxRowsA);
+                    const int bx = (kb % p.KBb) * BK;
+                    tma_load_2d(b_dst, &tm_b, fb, bx, b_y);
+                    if (EPI == EPI_SWIGLU) tma_load_2d(b_dst + 128 * 128, &tm_b2, fb, bx, b_y);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {  // let every copy this thread started land before the CTA exits
+                for (int s = 0; s < kStages; ++s)
+                    if (armed & (1u << s)) {
+                        volatile int never = 0;
+                        mbar_wait(full0 + 8 * s, (armed_parity >> s) & 1u, 1000000000LL, &never);
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------- MMA issuer
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            const uint32_t idesc = idesc_bf16(BM, p.BN);
+            bool ok = true;
+            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+                if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, lim, abort_flag)) {
+                    record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 2, blockIdx.x, u);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    if (!mbar_wait(full0 + 8 * stage, phase, lim, abort_flag)) {
+                        record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 3, blockIdx.x, u);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t ad = umma_desc(smem_u32(sA + stage * kABytes));
+                    const uint64_t bd = umma_desc(smem_u32(sB + stage * kBBytesMax));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)  // K=16 per MMA: 32 bytes along the swizzled row
+                        umma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                    umma_commit(empty0 + 8 * stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+                if (!ok) break;
+                umma_commit(tfull0 + 8 * acc);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1;
+                }
+            }
+            // every MMA this thread issued completes before TMEM is freed
+            umma_commit(drain);
+            volatile int never = 0;
+            mbar_wait(drain, 0, 1000000000LL, &never);
+        }
+    } else {
+        // ------------------------------------------------------- epilogue
+        const int sub = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = sub * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+            const Unit un = decode_unit(p, u);
+            int ok = 1;
+            if (lane == 0) {
+                ok = mbar_wait(tfull0 + 8 * acc, acc_phase, lim, abort_flag);
+                if (!ok) {
+                    record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 4, blockIdx.x, u);
+                    *abort_flag = 1;
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after();
+            const int m = un.m0 + row;
+            const bool valid = m < un.nrows;
+            const int64_t orow = (int64_t)un.row0 + m;
+            const uint32_t tb = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kAccCols);
+            if (EPI == EPI_SWIGLU) {
+                bf16* o = (bf16*)p.out + orow * p.ldo + un.nb * 128;
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 32) {
+                    uint32_t gr[32], ur[32];
+                    tmem_ld32(tb + c, gr);
+                    tmem_ld32(tb + 128 + c, ur);
+                    tmem_wait_ld();
+                    if (valid) {
+                        float h[32], lo[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) h[i] = swiglu(__uint_as_float(gr[i]), __uint_as_float(ur[i]));
+                        store_bf16x32(o + c, h);
+                        if (p.out_pair) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) lo[i] = h[i] - __bfloat162float(__float2bfloat16_rn(h[i]));
+                            store_bf16x32(o + p.N + c, lo);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll 1
+                for (int c = 0; c < p.BN; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(tb + c, r);
+                    tmem_wait_ld();
+                    if (valid) {
+                        const int n0 = un.nb * p.BN + c;
+                        if (p.out_f32) {
+                            float* o = (float*)p.out + orow * p.ldo + n0;
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) {
+                                float4 v = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
+                                                       __uint_as_float(r[i + 2]), __uint_as_float(r[i + 3]));
+                                if (p.bias) {
+                                    v.x += __ldg(p.bias + n0 + i);
+                                    v.y += __ldg(p.bias + n0 + i + 1);
+                                    v.z += __ldg(p.bias + n0 + i + 2);
+                                    v.w += __ldg(p.bias + n0 + i + 3);
+                                }
+                                *(float4*)(o + i) = v;
+                            }
+                        } else {
+                            float v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+                            store_bf16x32((bf16*)p.out + orow * p.ldo + n0, v);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * kAccCols)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------- host
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    });
+    return fn;
+}
+
+// 2D bf16 tensor [rows, cols] row-major, box {64 cols, box_rows}, 128B swizzle.
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn || rows < 1) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* q) { return ((uintptr_t)q & 15) == 0; }
+
+int plain_bn(int N) {
+    if (N % 256 == 0) return 256;
+    if (N <= 256 && N % 32 == 0) return N;
+    return 0;
+}
+
+}  // namespace tc
+
+bool gemm_tc_supported(const GroupedGemm& g) {
+    using namespace tc;
+    if (g.elem != kBF16) return false;
+    if (!encode_fn()) return false;
+    if (g.Ka % BK || g.Kb % BK || g.Ka < BK || g.Ka % g.Kb) return false;
+    if (!aligned16(g.a) || !aligned16(g.b) || !aligned16(g.out)) return false;
+    if (g.b2) {  // SwiGLU
+        if (g.N % 128 || g.out_elem != kBF16 || g.bias) return false;
+        if (!aligned16(g.b2) || (g.a_shared && !aligned16(g.a_shared))) return false;
+    } else {
+        if (!plain_bn(g.N) || g.out_pair) return false;
+        if (g.out_elem != kBF16 && g.out_elem != kF32) return false;
+        if (g.bias && g.out_elem != kF32) return false;
+    }
+    if (g.ldo % 8) return false;
+    return true;
+}
+
+cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t stream) {
+    using namespace tc;
+    const bool sw = g.b2 != nullptr;
+    Params p = {};
+    p.G = g.offsets ? g.G : 1;
+    p.shared_group = g.shared_group;
+    p.offsets = g.offsets;
+    p.tiles = g.tiles;
+    p.rows = g.rows;
+    p.BN = sw ? 256 : plain_bn(g.N);
+    p.NB = sw ? g.N / 128 : g.N / p.BN;
+    p.N = g.N;
+    p.KB = g.Ka / BK;
+    p.KBb = g.Kb / BK;
+    p.b_group_rows = g.N;
+    p.ldo = g.ldo;
+    p.out_pair = g.out_pair;
+    p.out_f32 = g.out_elem == kF32;
+    p.out = g.out;
+    p.bias = g.bias;
+    p.err = g.err;
+    p.spin_ns = g.spin_ns > 0 ? g.spin_ns : 2000000000LL;
+
+    CUtensorMap ma, msh, mb, mb2;
+    const int G = g.offsets ? g.G : 1;
+    if (!make_map(&ma, g.a, g.a_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
+    if (g.a_shared) {
+        if (!make_map(&msh, g.a_shared, g.a_shared_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
+    } else {
+        msh = ma;
+    }
+    const int brow_box = sw ? 128 : p.BN;
+    if (!make_map(&mb, g.b, (int64_t)G * g.N, g.Kb, brow_box)) return cudaErrorInvalidValue;
+    if (sw) {
+        if (!make_map(&mb2, g.b2, (int64_t)G * g.N, g.Kb, brow_box)) return cudaErrorInvalidValue;
+    } else {
+        mb2 = mb;
+    }
+    const int max_units = g.max_tiles * p.NB;
+    if (max_units <= 0) return cudaGetLastError();
+    const int grid = std::max(1, std::min(num_sms, max_units));
+    if (sw) {
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kSmemBytes);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        gemm_tc_kernel<EPI_SWIGLU><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, p);
+    } else {
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI_PLAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kSmemBytes);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        gemm_tc_kernel<EPI_PLAIN><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, p);
+    }
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 }  // namespace moe

@@ -27,7 +27,12 @@ struct GroupedGemm {
     const int32_t* tiles;        // [G+1] device prefix of ceil(rows/128) (nullptr with offsets)
     int rows;                    // single-group row count
     int max_tiles;               // host bound on the total number of row tiles
-    int N, K;
+    int N;                       // output columns (features) of one group
+    int Ka;                      // reduction length walked over A's row (= Kb, or 2*Kb for a hi/lo pair)
+    int Kb;                      // row length of B; B's column for reduction index k is k % Kb
+    int ldo;                     // output row stride in elements
+    int out_pair;                // 1: bf16 output split as hi | lo halves (hi at col n, lo at col N+n)
+    int a_rows, a_shared_rows;   // rows of the A tensors (tensor-map extents)
     int elem;                    // Elem of A and B
     const void* a;               // [*, K]
     const void* a_shared;        // [*, K]

@@ -112,7 +112,8 @@ class MoELayer:
         k, E, D, I = self.top_k, self.E, self.D, self.I
         TK, R = T * k, T * k + T
         act = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.uint8}[self.dtype]
-        ydt = torch.float32 if self.dtype == "f32" else torch.bfloat16
+        ydt = torch.bfloat16 if self.dtype == "fp8" else torch.float32
+        hcols = 2 * I if self.dtype == "bf16" else I
         v = {
             "err": self.ws_view(T, "err", torch.int32, (4,)),
             "logits": self.ws_view(T, "logits", torch.float32, (T, E)),
@@ -123,7 +124,7 @@ class MoELayer:
             "inv": self.ws_view(T, "inv", torch.int32, (TK,)),
             "src_tok": self.ws_view(T, "src_tok", torch.int32, (R,)),
             "xp": self.ws_view(T, "xp", act, (TK, D)),
-            "h": self.ws_view(T, "h", act, (R, I)),
+            "h": self.ws_view(T, "h", act, (R, hcols)),
             "y": self.ws_view(T, "y", ydt, (R, D)),
         }
         if self.dtype == "fp8":
