@@ -53,19 +53,25 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const TY* __restrict__ y
 #pragma unroll
             for (int i = 0; i < V; ++i) acc[i] = fmaf(wj, to_f32(e[i]), acc[i]);
         }
+        // This thread owns out[t, c .. c+V-1]: V*sizeof(TO) bytes at a
+        // multiple of that size (16 B for fp32 out, 8 or 16 B for bf16 out).
         TO* o = out + (int64_t)t * D + c;
         if constexpr (sizeof(TO) == 4) {
 #pragma unroll
             for (int i = 0; i < V; i += 4) *(float4*)(o + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+        } else if constexpr (V == 4) {
+            uint2 p;
+            __nv_bfloat162* pb = (__nv_bfloat162*)&p;
+            pb[0] = __floats2bfloat162_rn(acc[0], acc[1]);
+            pb[1] = __floats2bfloat162_rn(acc[2], acc[3]);
+            *(uint2*)o = p;
         } else {
+            static_assert(V == 8, "bf16 y carries 8 values per 16-byte vector");
+            uint4 p;
+            __nv_bfloat162* pb = (__nv_bfloat162*)&p;
 #pragma unroll
-            for (int i = 0; i < V; i += 8) {
-                uint4 p;
-                __nv_bfloat162* pb = (__nv_bfloat162*)&p;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) pb[q] = __floats2bfloat162_rn(acc[i + 2 * q], acc[i + 2 * q + 1]);
-                *(uint4*)(o + i) = p;
-            }
+            for (int q = 0; q < 4; ++q) pb[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+            *(uint4*)o = p;
         }
     }
 }
