@@ -59,7 +59,7 @@ def load_peaks():
 
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
 
@@ -67,6 +67,9 @@ class ClockSampler:
         self.proc = None
         self.path = f"/tmp/moe_clocks_{os.getpid()}.csv"
         self.gpu = gpu_index
+
+    def mark(self, name):
+        setattr(self, name, time.time())
 
     def __enter__(self):
         try:
@@ -90,15 +93,22 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        rows = []
+        import datetime
+        rows, inside = [], []
+        t0, t1 = getattr(self, "t_begin", 0.0), getattr(self, "t_end", 1e30)
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
             try:
-                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                r = (float(f[1]), float(f[2]), f[5], f[6], f[7], f[8])
             except ValueError:
                 continue
+            rows.append(r)
+            if t0 - 0.25 <= ts <= t1 + 0.25:
+                inside.append(r)
+        rows = inside or rows[-3:]
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
@@ -150,11 +160,6 @@ def run_ours(args, shape, world, rank, local):
     torch.cuda.set_device(dev)
     inp = synth.make_inputs(shape, seed=args.seed, device=dev)
     layer = MoELayer.from_shape(shape, inp, device=local)
-    # inputs the layer no longer needs (FP8: the fp32 originals)
-    if shape.dtype == "fp8":
-        for n in ("w_gate", "w_up", "w_down"):
-            inp[n] = None
-        torch.cuda.empty_cache()
     x = inp["x"]
     T = shape.T
     out = layer.new_out(T)
@@ -171,6 +176,8 @@ def run_ours(args, shape, world, rank, local):
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
+        time.sleep(0.3)  # let nvidia-smi start sampling
+        clk.mark("t_begin")
         t_start = torch.cuda.Event(enable_timing=True)
         t_end = torch.cuda.Event(enable_timing=True)
         t_start.record(stream)
@@ -190,6 +197,7 @@ def run_ours(args, shape, world, rank, local):
             e[5].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize(dev)
+        clk.mark("t_end")
     launches = L.moe_launch_count() - l0
     layer.check()
     ms_local = t_start.elapsed_time(t_end)
@@ -357,18 +365,23 @@ def run_reference(args, shape, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=synth.DECODE_BF16.name, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-tokens", type=int, default=24, help="oracle sample size for cpu_baseline")
+    ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample size for cpu_baseline")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override E (profiling captures on a few-GB copy of the workload); not a bench line")
     ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per step for --impl reference")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     shape = synth.WORKLOADS[args.workload]
+    if args.experts:
+        import dataclasses
+        shape = dataclasses.replace(shape, E=args.experts, name=f"{shape.name}_E{args.experts}_profile")
     world, rank, local = dist_env()
     if world > 1:
         backend = "nccl" if args.impl == "ours" else "gloo"

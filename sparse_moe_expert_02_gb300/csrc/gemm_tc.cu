@@ -39,13 +39,21 @@ namespace tc {
 
 constexpr int BM = 128;                   // rows per unit (TMEM lanes)
 constexpr int BK = 64;                    // K per stage: 64 bf16 = one 128-byte swizzle row
-constexpr int kStages = 4;
-constexpr int kABytes = BM * BK * 2;      // 16 KB
+constexpr int kABytes = BM * BK * 2;      // 16 KB: one A tile
 constexpr int kBBytesMax = 256 * BK * 2;  // 32 KB
 constexpr int kThreads = 192;
 constexpr int kAccCols = 256;             // TMEM columns per accumulator buffer
 constexpr int kBoxRowsA = 16;             // A is fetched in 16-row boxes (2 KB)
-constexpr uint32_t kSmemBytes = 1024 + kStages * (kABytes + kBBytesMax) + 256;
+constexpr uint32_t kSmemBytes = 1024 + 196608 + 256;
+
+// Stage geometry.  PAIR: A is a bf16 hi/lo pair (hi in columns [0, Kb), lo in
+// [Kb, 2Kb)); a stage holds the hi and lo tiles of one k-block next to one B
+// tile, so the weights stream once and both halves multiply the same tile.
+template <bool PAIR> struct Geo {
+    static constexpr int kStages = PAIR ? 3 : 4;
+    static constexpr int kAStage = PAIR ? 2 * kABytes : kABytes;
+    static_assert(kStages * (kAStage + kBBytesMax) <= 196608, "stage ring exceeds the smem budget");
+};
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_PLAIN = 1 };
 
@@ -57,8 +65,8 @@ struct Params {
     int NB;              // feature blocks per row tile
     int BN;              // MMA N (SwiGLU: 128 gate + 128 up)
     int N;               // output features of a group
-    int KB;              // k-blocks walked over A (Ka / 64)
-    int KBb;             // k-blocks of B (Kb / 64); B's k-block is kb % KBb
+    int KB;              // k-blocks of B (Kb / 64); one stage per k-block
+    int a_lo_x;          // PAIR: column where A's lo half starts (= Kb)
     int b_group_rows;    // rows of B per group
     int ldo;
     int out_pair;
@@ -195,15 +203,17 @@ __device__ __forceinline__ void store_bf16x32(bf16* dst, const float* v) {
 
 // ------------------------------------------------------------------ kernel
 
-template <int EPI>
+template <int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_sh,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
                    const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    constexpr int kStages = Geo<PAIR>::kStages;
+    constexpr int kAStage = Geo<PAIR>::kAStage;
     uint8_t* sA = smem;
-    uint8_t* sB = smem + kStages * kABytes;
+    uint8_t* sB = smem + kStages * kAStage;
     uint64_t* bars = (uint64_t*)(sB + kStages * kBBytesMax);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
     const uint32_t tfull0 = smem_u32(bars + 2 * kStages), tempty0 = smem_u32(bars + 2 * kStages + 2);
@@ -254,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int a_y = sh ? un.m0 : un.row0 + un.m0;
                 const int valid = min(BM, un.nrows - un.m0);
                 const int nbox = (valid + kBoxRowsA - 1) / kBoxRowsA;
-                const uint32_t bytes = (uint32_t)nbox * kBoxRowsA * BK * 2 + b_bytes;
+                const uint32_t bytes = (PAIR ? 2u : 1u) * (uint32_t)nbox * kBoxRowsA * BK * 2 + b_bytes;
                 const int b_y = un.g * p.b_group_rows + un.nb * ((EPI == EPI_SWIGLU) ? 128 : p.BN);
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, lim, abort_flag)) {
@@ -267,10 +277,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_expect_tx(fb, bytes);
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-                    const uint32_t a_dst = smem_u32(sA + stage * kABytes);
+                    const uint32_t a_dst = smem_u32(sA + stage * kAStage);
                     const uint32_t b_dst = smem_u32(sB + stage * kBBytesMax);
-                    for (int i = 0; i < nbox; ++i) tma_load_2d(a_dst + i * kBoxRowsA * 128, ta, fb, kb * BK, a_y + i * kBoxRowsA);
-                    const int bx = (kb % p.KBb) * BK;
+                    for (int i = 0; i < nbox; ++i) {
+                        tma_load_2d(a_dst + i * kBoxRowsA * 128, ta, fb, kb * BK, a_y + i * kBoxRowsA);
+                        if (PAIR)
+                            tma_load_2d(a_dst + kABytes + i * kBoxRowsA * 128, ta, fb, p.a_lo_x + kb * BK,
+                                        a_y + i * kBoxRowsA);
+                    }
+                    const int bx = kb * BK;
                     tma_load_2d(b_dst, &tm_b, fb, bx, b_y);
                     if (EPI == EPI_SWIGLU) tma_load_2d(b_dst + 128 * 128, &tm_b2, fb, bx, b_y);
                     if (++stage == kStages) {
@@ -311,11 +326,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t ad = umma_desc(smem_u32(sA + stage * kABytes));
+                    const uint64_t ad = umma_desc(smem_u32(sA + stage * kAStage));
                     const uint64_t bd = umma_desc(smem_u32(sB + stage * kBBytesMax));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)  // K=16 per MMA: 32 bytes along the swizzled row
                         umma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                    if (PAIR) {
+                        const uint64_t al = umma_desc(smem_u32(sA + stage * kAStage + kABytes));
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            umma_bf16(d, al + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, 1u);
+                    }
                     umma_commit(empty0 + 8 * stage);
                     if (++stage == kStages) {
                         stage = 0;
@@ -466,13 +487,28 @@ int plain_bn(int N) {
     return 0;
 }
 
+template <int EPI, bool PAIR>
+cudaError_t launch_one(int grid, const CUtensorMap& ma, const CUtensorMap& msh, const CUtensorMap& mb,
+                       const CUtensorMap& mb2, const Params& p, cudaStream_t stream) {
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    gemm_tc_kernel<EPI, PAIR><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, p);
+    return cudaGetLastError();
+}
+
 }  // namespace tc
 
 bool gemm_tc_supported(const GroupedGemm& g) {
     using namespace tc;
     if (g.elem != kBF16) return false;
     if (!encode_fn()) return false;
-    if (g.Ka % BK || g.Kb % BK || g.Ka < BK || g.Ka % g.Kb) return false;
+    if (g.Kb % BK || g.Kb < BK || (g.Ka != g.Kb && g.Ka != 2 * g.Kb)) return false;
+    if (g.b2 && g.Ka != g.Kb) return false;  // the hi/lo pair is only the down GEMM's input
     if (!aligned16(g.a) || !aligned16(g.b) || !aligned16(g.out)) return false;
     if (g.b2) {  // SwiGLU
         if (g.N % 128 || g.out_elem != kBF16 || g.bias) return false;
@@ -486,9 +522,11 @@ bool gemm_tc_supported(const GroupedGemm& g) {
     return true;
 }
 
+
 cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t stream) {
     using namespace tc;
     const bool sw = g.b2 != nullptr;
+    const bool pair = g.Ka == 2 * g.Kb;
     Params p = {};
     p.G = g.offsets ? g.G : 1;
     p.shared_group = g.shared_group;
@@ -496,10 +534,17 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     p.tiles = g.tiles;
     p.rows = g.rows;
     p.BN = sw ? 256 : plain_bn(g.N);
+    if (!sw && !g.offsets) {
+        // single group (router): narrow the feature block until the units
+        // cover the SMs (T=128 at E=512: 16 units of 32 experts, not 2 of 256)
+        const int row_tiles = (g.rows + BM - 1) / BM;
+        while (p.BN > 32 && g.N % (p.BN / 2) == 0 && (p.BN / 2) % 32 == 0 && row_tiles * (g.N / p.BN) < num_sms)
+            p.BN /= 2;
+    }
     p.NB = sw ? g.N / 128 : g.N / p.BN;
     p.N = g.N;
-    p.KB = g.Ka / BK;
-    p.KBb = g.Kb / BK;
+    p.KB = g.Kb / BK;
+    p.a_lo_x = g.Kb;
     p.b_group_rows = g.N;
     p.ldo = g.ldo;
     p.out_pair = g.out_pair;
@@ -527,27 +572,12 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     const int max_units = g.max_tiles * p.NB;
     if (max_units <= 0) return cudaGetLastError();
     const int grid = std::max(1, std::min(num_sms, max_units));
-    if (sw) {
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI_SWIGLU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kSmemBytes);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
-        gemm_tc_kernel<EPI_SWIGLU><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, p);
-    } else {
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI_PLAIN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kSmemBytes);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
-        gemm_tc_kernel<EPI_PLAIN><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, p);
-    }
+    cudaError_t e;
+    if (sw) e = launch_one<EPI_SWIGLU, false>(grid, ma, msh, mb, mb2, p, stream);
+    else if (pair) e = launch_one<EPI_PLAIN, true>(grid, ma, msh, mb, mb2, p, stream);
+    else e = launch_one<EPI_PLAIN, false>(grid, ma, msh, mb, mb2, p, stream);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe
