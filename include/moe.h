@@ -200,6 +200,31 @@ MOE_API moe_status moe_gemm_down(const moe_plan* plan, const moe_weights* w, int
  * reduction). */
 MOE_API moe_status moe_unpermute(const moe_plan* plan, int32_t T, void* out, void* ws, size_t ws_bytes, void* stream);
 
+/* Allocation-free permutation index build (no counterpart in the paper:
+ * it exists for callers of this library that cannot allocate device memory,
+ * e.g. a plugin whose host framework owns every device allocation through
+ * its own arena, or a serving loop that forbids cudaMalloc -- and the device
+ * synchronisation it may cause -- after start-up).
+ * Computes what moe_permute writes into counts, offsets, tiles, inv and
+ * src_tok, from idx = the [T, top_k] expert-index plane, with the same
+ * kernels; the caller passes those outputs ([E+1], [E+2], [E+2], [T*top_k],
+ * [T*top_k + T] int32, device pointers).  No allocation of any kind: the
+ * only scratch (per-chunk histograms) is one 1 MiB array in the library's
+ * device memory, held by every GPU that loads the library until the process
+ * exits; so ceil(T*top_k / 1024) * E must not exceed 262144 (e.g. E=512
+ * allows T*top_k <= 524288), else MOE_ERR_UNSUPPORTED before any work.
+ * E <= 1024, 1 <= top_k <= min(E, 32).
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress (with that device current); make that first call
+ * before any stream capture.  Every call on a device shares the one array:
+ * calls that overlap on the GPU (other streams, other threads) race and must
+ * be serialised by the caller.  Out-of-range expert ids are skipped (their
+ * pairs get no row); there is no error word.  The array keeps the last
+ * call's histograms, which no later call reads before overwriting. */
+MOE_API moe_status moe_permute_index_noalloc(const int32_t* idx, int32_t T, int32_t E, int32_t top_k,
+                                             int32_t* counts, int32_t* offsets, int32_t* tiles, int32_t* inv,
+                                             int32_t* src_tok, void* stream);
+
 /* Synchronise `stream`, read the workspace error word and return the first
  * device-side error recorded since the last clear (MOE_OK if none). */
 MOE_API moe_status moe_check(const moe_plan* plan, const void* ws, void* stream);

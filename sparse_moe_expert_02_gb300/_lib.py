@@ -34,6 +34,7 @@ SYMBOLS = (
     "moe_workspace_init", "moe_quantize_weights", "moe_forward", "moe_route", "moe_topk", "moe_permute",
     "moe_gemm_gateup", "moe_gemm_down", "moe_unpermute", "moe_check", "moe_selftest_wait_timeout",
     "moe_status_str", "moe_last_error_detail", "moe_build_info", "moe_launch_count",
+    "moe_permute_index_noalloc",
 )
 
 
@@ -97,6 +98,7 @@ def lib():
                 "moe_last_error_detail": (ctypes.c_char_p, []),
                 "moe_build_info": (ctypes.c_char_p, []),
                 "moe_launch_count": (ctypes.c_uint64, []),
+                "moe_permute_index_noalloc": (st, [P, I32, I32, I32, P, P, P, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -217,6 +219,12 @@ def moe_check_status(plan, ws, stream=None) -> int:
 def moe_selftest_wait_timeout(plan, ws, limit_ns: int, stream=None):
     _ok(lib().moe_selftest_wait_timeout(plan, _ptr(ws), _wsb(ws), limit_ns, _stream(stream)),
         "moe_selftest_wait_timeout")
+
+
+def moe_permute_index_noalloc(idx, T, E, top_k, counts, offsets, tiles, inv, src_tok, stream=None) -> int:
+    """Allocation-free permutation index build; returns the moe_status."""
+    return lib().moe_permute_index_noalloc(_ptr(idx), T, E, top_k, _ptr(counts), _ptr(offsets), _ptr(tiles),
+                                           _ptr(inv), _ptr(src_tok), _stream(stream))
 
 
 def moe_launch_count() -> int:

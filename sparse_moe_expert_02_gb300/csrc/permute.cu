@@ -15,6 +15,7 @@
 //              experts inside each 32-pair step with __match_any_sync, and
 //              writes inv[pair] and src_tok[row].
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -256,3 +257,60 @@ cudaError_t launch_quant_blocks(const float* w, int64_t groups, int rows, int co
 }
 
 }  // namespace moe
+
+// ------------------------------------------------- allocation-free variant
+//
+// Some callers cannot call cudaMalloc at all: a plugin inside a host
+// framework that owns every byte of device memory through its own arena, or
+// a serving loop that forbids allocation (and the device synchronisation it
+// can imply) once it has started.  They still pass their inputs and outputs;
+// the only extra memory the permutation index build needs -- the per-chunk
+// expert histograms -- lives here, in one file-scope device array that every
+// GPU loading this library holds until the process exits.
+
+namespace moe {
+namespace {
+
+constexpr int kNoAllocHistInts = 1 << 18;  // 1 MiB: chunks * E <= 262144
+constexpr int kNoAllocMaxDevices = 64;
+
+static __device__ __align__(256) int32_t g_noalloc_hist[kNoAllocHistInts];
+
+std::mutex g_noalloc_mu;
+int32_t* g_noalloc_addr[kNoAllocMaxDevices] = {};
+
+}  // namespace
+
+}  // namespace moe
+
+extern "C" MOE_API moe_status moe_permute_index_noalloc(const int32_t* idx, int32_t T, int32_t E, int32_t top_k,
+                                                        int32_t* counts, int32_t* offsets, int32_t* tiles,
+                                                        int32_t* inv, int32_t* src_tok, void* stream) {
+    using namespace moe;
+    if (!idx || !counts || !offsets || !tiles || !inv || !src_tok) return MOE_ERR_INVALID_ARG;
+    if (T < 1 || E < 1 || E > 1024 || top_k < 1 || top_k > 32 || top_k > E) return MOE_ERR_INVALID_ARG;
+    if ((int64_t)T * (top_k + 1) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+    const int64_t chunks = cdiv((int64_t)T * top_k, kPermChunk);
+    if (chunks * E > kNoAllocHistInts) return MOE_ERR_UNSUPPORTED;  // beyond the static scratch
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_CUDA;
+    int32_t* hist = nullptr;
+    {
+        // First call on this device: look up the array's device address
+        // (the host-side name is only a stand-in, not a device pointer).
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_addr[dev]) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_hist) != cudaSuccess || !p) return MOE_ERR_CUDA;
+            g_noalloc_addr[dev] = (int32_t*)p;
+        }
+        hist = g_noalloc_addr[dev];
+    }
+    // Every histogram entry a chunk uses is written by the hist kernel before
+    // the scan reads it, so what an earlier call left in the array is never
+    // read and nothing needs clearing.
+    if (launch_permute_index(idx, T, E, top_k, hist, counts, offsets, tiles, inv, src_tok, nullptr,
+                             (cudaStream_t)stream) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
