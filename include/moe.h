@@ -139,6 +139,7 @@ typedef struct moe_ws_layout {
                           R = T*top_k + T */
     size_t h_scale;    /* FP8: f32 [T*top_k + T, I/128] */
     size_t y;          /* [R, D] expert outputs: f32 (MOE_F32, MOE_BF16) or bf16 (FP8 layer) */
+    size_t logits_part;/* f32 [S, T, E] router K-slice partials when T is small (S > 1), else 0 */
 } moe_ws_layout;
 
 /* Validate a configuration and build a host-side plan for `device`.

@@ -52,7 +52,7 @@ class moe_weights(ctypes.Structure):
 class moe_ws_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("total", "err", "logits", "blob", "counts", "offsets", "tiles", "inv", "src_tok", "hist", "xq",
-                 "xq_scale", "xp", "xp_scale", "h", "h_scale", "y")]
+                 "xq_scale", "xp", "xp_scale", "h", "h_scale", "y", "logits_part")]
 
 
 class MoEError(RuntimeError):

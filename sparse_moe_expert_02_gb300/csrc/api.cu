@@ -47,7 +47,11 @@ int act_bytes(int dtype) { return dtype == MOE_F32 ? 4 : (dtype == MOE_BF16 ? 2 
 int act_elem(int dtype) { return dtype == MOE_F32 ? moe::kF32 : (dtype == MOE_BF16 ? moe::kBF16 : moe::kE4M3); }
 int in_elem(int dtype) { return dtype == MOE_F32 ? moe::kF32 : moe::kBF16; }  // x and router
 
-void layout(const moe_config& c, int T, moe_ws_layout* L) {
+int route_splits(const moe_config& c, int T, int num_sms) {
+    return c.dtype == MOE_F32 ? 1 : moe::router_splits(T, c.E, c.D, num_sms);
+}
+
+void layout(const moe_config& c, int num_sms, int T, moe_ws_layout* L) {
     const int64_t TK = (int64_t)T * c.top_k, R = TK + T;
     const bool fp8 = c.dtype == MOE_FP8_E4M3_B128;
     const int ab = act_bytes(c.dtype);
@@ -76,6 +80,8 @@ void layout(const moe_config& c, int T, moe_ws_layout* L) {
     // y in fp32 except for the FP8 layer (bf16 there): a bf16 y alone costs
     // about 1.3e-2 of the output rms, above the bf16 layer's tolerance.
     L->y = take((size_t)R * c.D * (c.dtype == MOE_FP8_E4M3_B128 ? 2 : 4));
+    const int S = route_splits(c, T, num_sms);
+    L->logits_part = S > 1 ? take((size_t)S * T * c.E * 4) : 0;
     L->total = o;
 }
 
@@ -89,7 +95,7 @@ moe_status check_call(const moe_plan* p, int32_t T, void* ws, size_t ws_bytes, W
     if (!p) return arg_fail(MOE_ERR_INVALID_ARG, "plan is NULL");
     if (T < 1 || T > p->cfg.T_max) return arg_fail(MOE_ERR_INVALID_ARG, "T outside [1, T_max]");
     if (!ws || !aligned(ws, 256)) return arg_fail(MOE_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
-    layout(p->cfg, T, &out->L);
+    layout(p->cfg, p->num_sms, T, &out->L);
     if (ws_bytes < out->L.total) return arg_fail(MOE_ERR_WORKSPACE, "workspace smaller than moe_workspace_size()");
     out->base = (char*)ws;
     int cur = -1;
@@ -198,7 +204,7 @@ const moe_config* moe_plan_config(const moe_plan* p) { return p ? &p->cfg : null
 moe_status moe_workspace_layout(const moe_plan* p, int32_t T, moe_ws_layout* out) {
     if (!p || !out) return arg_fail(MOE_ERR_INVALID_ARG, "NULL argument");
     if (T < 1 || T > p->cfg.T_max) return arg_fail(MOE_ERR_INVALID_ARG, "T outside [1, T_max]");
-    layout(p->cfg, T, out);
+    layout(p->cfg, p->num_sms, T, out);
     return MOE_OK;
 }
 
@@ -231,8 +237,8 @@ moe_status moe_topk(const moe_plan* p, int32_t T, void* ws, size_t ws_bytes, voi
     moe_status st = check_call(p, T, ws, ws_bytes, &W);
     if (st != MOE_OK) return st;
     const moe_config& c = p->cfg;
-    MOE_CUDA(moe::launch_topk(W.at<float>(W.L.logits), T, c.E, c.top_k, W.at<int32_t>(W.L.blob),
-                              W.at<uint32_t>(W.L.err), (cudaStream_t)stream));
+    MOE_CUDA(moe::launch_topk(W.at<float>(W.L.logits), 1, nullptr, nullptr, T, c.E, c.top_k,
+                              W.at<int32_t>(W.L.blob), W.at<uint32_t>(W.L.err), (cudaStream_t)stream));
     return MOE_OK;
 }
 
@@ -261,8 +267,24 @@ moe_status moe_route(const moe_plan* p, const moe_weights* w, const void* x, int
     g.bias = c.has_router_bias ? w->b_router : nullptr;
     g.err = W.at<uint32_t>(W.L.err);
     g.spin_ns = p->spin_ns;
+    // Small T: split K over several CTAs; the top-k kernel then adds the
+    // slices in order (and the bias) and writes the logits.
+    const int S = use_tc(p, g) ? route_splits(c, T, p->num_sms) : 1;
+    if (S > 1) {
+        g.ksplit = S;
+        g.split_stride = (int64_t)T * c.E;
+        g.out = W.at<float>(W.L.logits_part);
+        g.bias = nullptr;
+    }
     if ((st = run_gemm(p, g, (cudaStream_t)stream, "router GEMM")) != MOE_OK) return st;
-    return moe_topk(p, T, ws, ws_bytes, stream);
+    if (S > 1)
+        MOE_CUDA(moe::launch_topk(W.at<float>(W.L.logits_part), S, c.has_router_bias ? w->b_router : nullptr,
+                                  W.at<float>(W.L.logits), T, c.E, c.top_k, W.at<int32_t>(W.L.blob),
+                                  W.at<uint32_t>(W.L.err), (cudaStream_t)stream));
+    else
+        MOE_CUDA(moe::launch_topk(W.at<float>(W.L.logits), 1, nullptr, nullptr, T, c.E, c.top_k,
+                                  W.at<int32_t>(W.L.blob), W.at<uint32_t>(W.L.err), (cudaStream_t)stream));
+    return MOE_OK;
 }
 
 moe_status moe_permute(const moe_plan* p, const void* x, int32_t T, void* ws, size_t ws_bytes, void* stream) {

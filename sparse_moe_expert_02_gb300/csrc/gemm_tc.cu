@@ -66,6 +66,8 @@ struct Params {
     int BN;              // MMA N (SwiGLU: 128 gate + 128 up)
     int N;               // output features of a group
     int KB;              // k-blocks of B (Kb / 64); one stage per k-block
+    int KS;              // K slices (single group only): slice s walks k-blocks [s*KB/KS, (s+1)*KB/KS)
+    int64_t split_stride;  // elements between the outputs of two K slices
     int a_lo_x;          // PAIR: column where A's lo half starts (= Kb)
     int b_group_rows;    // rows of B per group
     int ldo;
@@ -169,11 +171,15 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 // ------------------------------------------------------------ unit decode
 
 struct Unit {
-    int g, m0, row0, nrows, nb;
+    int g, m0, row0, nrows, nb, ks;
 };
 
-__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+// Units: K slice major, then row tile, then feature block.
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u, int total_tiles) {
     Unit r;
+    const int per_slice = total_tiles * p.NB;
+    r.ks = u / per_slice;
+    u -= r.ks * per_slice;
     const int rt = u / p.NB;
     r.nb = u - rt * p.NB;
     if (p.offsets) {
@@ -247,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     const int total_tiles = p.offsets ? __ldg(p.tiles + p.G) : (p.rows + BM - 1) / BM;
-    const int total_units = total_tiles * p.NB;
+    const int total_units = total_tiles * p.NB * p.KS;
+    const int kbs = p.KB / p.KS;  // k-blocks per unit
     const int64_t lim = p.spin_ns;
 
     if (warp == 0) {
@@ -258,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b_bytes = (EPI == EPI_SWIGLU) ? 2u * 128 * BK * 2 : (uint32_t)p.BN * BK * 2;
             bool ok = true;
             for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-                const Unit un = decode_unit(p, u);
+                const Unit un = decode_unit(p, u, total_tiles);
                 const bool sh = un.g == p.shared_group;
                 const CUtensorMap* ta = sh ? &tm_a_sh : &tm_a;
                 const int a_y = sh ? un.m0 : un.row0 + un.m0;
@@ -266,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nbox = (valid + kBoxRowsA - 1) / kBoxRowsA;
                 const uint32_t bytes = (PAIR ? 2u : 1u) * (uint32_t)nbox * kBoxRowsA * BK * 2 + b_bytes;
                 const int b_y = un.g * p.b_group_rows + un.nb * ((EPI == EPI_SWIGLU) ? 128 : p.BN);
-                for (int kb = 0; kb < p.KB; ++kb) {
+                for (int kb = un.ks * kbs; kb < (un.ks + 1) * kbs; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, lim, abort_flag)) {
                         record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 1, blockIdx.x, u);
                         *abort_flag = 1;
@@ -318,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d = tmem_base + (uint32_t)(acc * kAccCols);
-                for (int kb = 0; kb < p.KB; ++kb) {
+                for (int kb = 0; kb < kbs; ++kb) {
                     if (!mbar_wait(full0 + 8 * stage, phase, lim, abort_flag)) {
                         record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 3, blockIdx.x, u);
                         *abort_flag = 1;
@@ -362,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-            const Unit un = decode_unit(p, u);
+            const Unit un = decode_unit(p, u, total_tiles);
             int ok = 1;
             if (lane == 0) {
                 ok = mbar_wait(tfull0 + 8 * acc, acc_phase, lim, abort_flag);
@@ -407,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (valid) {
                         const int n0 = un.nb * p.BN + c;
                         if (p.out_f32) {
-                            float* o = (float*)p.out + orow * p.ldo + n0;
+                            float* o = (float*)p.out + un.ks * p.split_stride + orow * p.ldo + n0;
 #pragma unroll
                             for (int i = 0; i < 32; i += 4) {
                                 float4 v = make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]),
@@ -544,6 +551,9 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     p.NB = sw ? g.N / 128 : g.N / p.BN;
     p.N = g.N;
     p.KB = g.Kb / BK;
+    p.KS = 1;
+    if (!g.offsets && g.ksplit > 1 && p.KB % g.ksplit == 0) p.KS = g.ksplit;
+    p.split_stride = g.split_stride;
     p.a_lo_x = g.Kb;
     p.b_group_rows = g.N;
     p.ldo = g.ldo;
@@ -569,7 +579,7 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     } else {
         mb2 = mb;
     }
-    const int max_units = g.max_tiles * p.NB;
+    const int max_units = g.max_tiles * p.NB * p.KS;
     if (max_units <= 0) return cudaGetLastError();
     const int grid = std::max(1, std::min(num_sms, max_units));
     cudaError_t e;

@@ -46,6 +46,9 @@ struct GroupedGemm {
     int out_elem;                // Elem of out (kE4M3: out_scale receives [*, N/128])
     float* out_scale;
     const float* bias;           // [N] added to the result (router) or nullptr
+    int ksplit;                  // single group only: K split into this many slices (0/1: none);
+                                 // slice s writes its partial product at out + s * split_stride
+    int64_t split_stride;
     uint32_t* err;
     int64_t spin_ns;
 };
@@ -59,8 +62,11 @@ cudaError_t launch_gemm_simt(const GroupedGemm& g, cudaStream_t stream);
 cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t stream);
 bool gemm_tc_supported(const GroupedGemm& g);
 
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* blob, uint32_t* err,
-                        cudaStream_t stream);
+// Top-k over logits = sum_{s<S} part[s] (+ bias), summed in slice order;
+// when S > 1 or bias is given the summed logits are written to logits_out.
+cudaError_t launch_topk(const float* part, int S, const float* bias, float* logits_out, int T, int E, int k,
+                        int32_t* blob, uint32_t* err, cudaStream_t stream);
+int router_splits(int T, int E, int D, int num_sms);
 
 cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_t* hist, int32_t* counts,
                                  int32_t* offsets, int32_t* tiles, int32_t* inv, int32_t* src_tok, uint32_t* err,

@@ -11,25 +11,37 @@
 // expert index on equal logits -- the same total order in every lane and in
 // the cross-lane reduction, so the choice is deterministic.  Weights are the
 // softmax over the chosen logits (equal to the renormalised full softmax).
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 
 template <int J>  // J = ceil(E / 32) logits per lane
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
-                                                   int32_t* __restrict__ blob, uint32_t* err) {
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int S,
+                                                   const float* __restrict__ bias, float* __restrict__ logits_out,
+                                                   int T, int E, int k, int32_t* __restrict__ blob, uint32_t* err) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
-    const float* zt = logits + (int64_t)t * E;
+    const int64_t TE = (int64_t)T * E;
+    const float* zt = part + (int64_t)t * E;
     float v[J];
     bool finite = true;
 #pragma unroll
     for (int j = 0; j < J; ++j) {
-        int e = lane + 32 * j;
-        v[j] = (e < E) ? __ldg(zt + e) : 0.0f;
-        if (e < E && !isfinite(v[j])) finite = false;
+        const int e = lane + 32 * j;
+        float z = 0.0f;
+        if (e < E) {
+            // K-split partial products of the router GEMM, added in slice order
+            z = __ldg(zt + e);
+            for (int s = 1; s < S; ++s) z += __ldg(zt + s * TE + e);
+            if (bias) z += __ldg(bias + e);
+            if (logits_out) logits_out[(int64_t)t * E + e] = z;
+        }
+        v[j] = z;
+        if (e < E && !isfinite(z)) finite = false;
     }
     if (!__all_sync(0xffffffffu, finite)) {
         if (lane == 0) record_error(err, MOE_ERR_NONFINITE, (uint32_t)t, 0, 0);
@@ -75,19 +87,31 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     }
 }
 
-cudaError_t launch_topk(const float* logits, int T, int E, int k, int32_t* blob, uint32_t* err,
-                        cudaStream_t stream) {
+cudaError_t launch_topk(const float* part, int S, const float* bias, float* logits_out, int T, int E, int k,
+                        int32_t* blob, uint32_t* err, cudaStream_t stream) {
     const int warps = 8;
     dim3 grid((unsigned)cdiv(T, warps)), block(32 * warps);
-    int J = (int)cdiv(E, 32);
-    if (J <= 1) topk_kernel<1><<<grid, block, 0, stream>>>(logits, T, E, k, blob, err);
-    else if (J <= 2) topk_kernel<2><<<grid, block, 0, stream>>>(logits, T, E, k, blob, err);
-    else if (J <= 4) topk_kernel<4><<<grid, block, 0, stream>>>(logits, T, E, k, blob, err);
-    else if (J <= 8) topk_kernel<8><<<grid, block, 0, stream>>>(logits, T, E, k, blob, err);
-    else if (J <= 16) topk_kernel<16><<<grid, block, 0, stream>>>(logits, T, E, k, blob, err);
-    else topk_kernel<32><<<grid, block, 0, stream>>>(logits, T, E, k, blob, err);
+    const int J = (int)cdiv(E, 32);
+#define MOE_TOPK(JJ) topk_kernel<JJ><<<grid, block, 0, stream>>>(part, S, bias, logits_out, T, E, k, blob, err)
+    if (J <= 1) MOE_TOPK(1);
+    else if (J <= 2) MOE_TOPK(2);
+    else if (J <= 4) MOE_TOPK(4);
+    else if (J <= 8) MOE_TOPK(8);
+    else if (J <= 16) MOE_TOPK(16);
+    else MOE_TOPK(32);
+#undef MOE_TOPK
     count_launches(1);
     return cudaGetLastError();
+}
+
+// K slices of the router GEMM: enough (up to 8) that the units of 32
+// experts x 128 tokens x K/S cover the SMs when T is small.
+int router_splits(int T, int E, int D, int num_sms) {
+    const int units = (int)cdiv(T, 128) * std::max(1, E / 32);
+    const int kblocks = D / 64;
+    int S = 1;
+    while (S < 8 && units * S * 2 <= num_sms && kblocks % (2 * S) == 0) S *= 2;
+    return S;
 }
 
 }  // namespace moe
