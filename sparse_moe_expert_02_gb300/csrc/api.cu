@@ -55,7 +55,7 @@ void layout(const moe_config& c, int num_sms, int T, moe_ws_layout* L) {
     const int64_t TK = (int64_t)T * c.top_k, R = TK + T;
     const bool fp8 = c.dtype == MOE_FP8_E4M3_B128;
     const int ab = act_bytes(c.dtype);
-    const int64_t nch = moe::cdiv(TK, moe::kPermChunk);
+    const int64_t nch = moe::cdiv(TK, moe::perm_chunk(TK));
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o += up256(bytes); return at; };
     memset(L, 0, sizeof(*L));
@@ -128,6 +128,12 @@ bool use_tc(const moe_plan* p, const moe::GroupedGemm& g) {
 }
 
 moe_status run_gemm(const moe_plan* p, const moe::GroupedGemm& g, cudaStream_t s, const char* what) {
+    if (g.elem == moe::kE4M3) {
+        if (!moe::gemm_fp8_supported(g)) return arg_fail(MOE_ERR_UNSUPPORTED, "FP8 GEMM shape without a kernel");
+        cudaError_t e = moe::launch_gemm_fp8(g, p->num_sms, s);
+        if (e != cudaSuccess) return cuda_fail(e, what);
+        return MOE_OK;
+    }
     if (use_tc(p, g)) {
         MOE_CUDA(moe::launch_gemm_tc(g, p->num_sms, s));
         return MOE_OK;

@@ -1,0 +1,471 @@
+// Grouped GEMM with E4M3 operands and fp32 block scales on the tcgen05
+// tensor cores (the FP8 layer's expert GEMMs).
+//
+// "Systems engineering playbook: Qwen 3.5 MoE on Ironwood TPU" (English page,
+// "Roofline Validation"): FP8 scaling blocks, audited against a
+// higher-precision path.  Here: weights carry one fp32 scale per 128x128
+// block, activations one per token per 128 columns, so every 128-wide slice
+// of K has its own product of scales.  tcgen05.mma kind::f8f6f4 multiplies
+// one such slice (4 MMAs of K=32) into one of two TMEM chunk buffers; the
+// epilogue warps read the chunk, multiply it by s_a[row] * s_w[block] and add
+// it to fp32 accumulators held in registers, while the MMA fills the other
+// buffer.  The scales are not powers of two, so they cannot ride in the
+// MMA's own block-scale operands.
+//
+// Unit, ordering, ring and error handling follow gemm_tc.cu (128 rows x 256
+// accumulator columns; A in 16-row TMA boxes; 4-stage ring of 16 KB A + 32 KB
+// B; bounded waits).  384 threads in three warpgroups: warp 0 TMA, warp 1
+// TMEM + MMA, warps 2-3 idle; warps 4..11 epilogue (two per TMEM lane
+// quarter, each owning half of the columns).  The block launches at 168
+// registers per thread; warpgroup 0 gives back down to 40 and the two
+// epilogue warpgroups take up to 232 (4*32*128 = 8*32*64 registers, so the
+// split balances exactly) for their 128 fp32 accumulators.
+//   SwiGLU (gate/up): columns 0..127 gate, 128..255 up, features nb*128..+127.
+//     A thread owns 64 gate and the matching 64 up columns of its row; at the
+//     end of the unit it forms h, the two halves of a row exchange their amax
+//     through shared memory, and h is written as E4M3 codes with one fp32
+//     scale per row and 128 features (the next GEMM's activation format).
+//   Plain (down): 256 output features = two 128-row weight blocks, one per
+//     column half; the result is written as bf16.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace tc {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn();  // gemm_tc.cu
+
+namespace f8 {
+
+constexpr int BM = 128;
+constexpr int BKB = 128;                  // K per stage: 128 E4M3 = one 128-byte swizzle row
+constexpr int kStages = 4;
+constexpr int kABytes = BM * BKB;         // 16 KB
+constexpr int kBBytes = 256 * BKB;        // 32 KB
+constexpr int kEpiWarps = 8;
+constexpr int kEpiWarp0 = 4;              // first epilogue warp (warpgroups 1 and 2)
+constexpr int kThreads = 128 + 32 * kEpiWarps;
+constexpr int kRegsLaunch = 168, kRegsLow = 40, kRegsHigh = 232;
+static_assert(4 * (kRegsLaunch - kRegsLow) == kEpiWarps * (kRegsHigh - kRegsLaunch), "register split must balance");
+static_assert(kThreads * kRegsLaunch <= 65536, "launch registers exceed the SM");
+constexpr int kAccCols = 256;
+constexpr int kBoxRowsA = 16;
+constexpr uint32_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + 256 + 2 * 2 * 128 * 4;
+
+enum Epi : int { EPI_SWIGLU = 0, EPI_PLAIN = 1 };
+
+struct Params {
+    int G, shared_group;
+    const int32_t* offsets;
+    const int32_t* tiles;
+    int NB;               // feature blocks per row tile
+    int N;                // output features of a group
+    int KB;               // 128-wide K chunks
+    const float* a_scale;         // [rows of A, KB]
+    const float* a_shared_scale;  // [rows of A_shared, KB]
+    const float* b_scale;         // [G, N/128, KB]
+    const float* b2_scale;
+    void* out;
+    int ldo;                      // output row stride in elements
+    float* out_scale;             // SwiGLU: [R, N/128]
+    uint32_t* err;
+    int64_t spin_ns;
+};
+
+struct Unit {
+    int g, m0, row0, nrows, nb;
+};
+
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+    Unit r;
+    const int rt = u / p.NB;
+    r.nb = u - rt * p.NB;
+    r.g = find_group(p.tiles, p.G, rt);
+    r.m0 = (rt - __ldg(p.tiles + r.g)) * BM;
+    r.row0 = __ldg(p.offsets + r.g);
+    r.nrows = __ldg(p.offsets + r.g + 1) - r.row0;
+    return r;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_sh,
+                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
+                    const Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + kStages * kABytes;
+    uint64_t* bars = (uint64_t*)(sB + kStages * kBBytes);
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
+    const uint32_t cfull0 = smem_u32(bars + 2 * kStages), cempty0 = smem_u32(bars + 2 * kStages + 2);
+    const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
+    const uint32_t xbar0 = smem_u32(bars + 2 * kStages + 5);  // [2]: amax exchange, one per unit parity
+    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kStages + 7);
+    volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+    float* s_amax = (float*)(smem + kStages * (kABytes + kBBytes) + 256);  // [2 units][2 halves][128 rows]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(cfull0 + 8 * b, 1);
+            mbar_init(cempty0 + 8 * b, kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        mbar_init(xbar0, kEpiWarps * 32);
+        mbar_init(xbar0 + 8, kEpiWarps * 32);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(2 * kAccCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int total_units = __ldg(p.tiles + p.G) * p.NB;
+    const int64_t lim = p.spin_ns;
+
+    if (warp < kEpiWarp0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------------- TMA producer
+            int stage = 0;
+            uint32_t phase = 0, armed = 0, armed_parity = 0;
+            constexpr uint32_t b_bytes = 256u * BKB;
+            bool ok = true;
+            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+                const Unit un = decode_unit(p, u);
+                const bool sh = un.g == p.shared_group;
+                const CUtensorMap* ta = sh ? &tm_a_sh : &tm_a;
+                const int a_y = sh ? un.m0 : un.row0 + un.m0;
+                const int valid = min(BM, un.nrows - un.m0);
+                const int nbox = (valid + kBoxRowsA - 1) / kBoxRowsA;
+                const uint32_t bytes = (uint32_t)nbox * kBoxRowsA * BKB + b_bytes;
+                const int b_y = un.g * p.N + un.nb * ((EPI == EPI_SWIGLU) ? 128 : 256);
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, lim, abort_flag)) {
+                        record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 11, blockIdx.x, u);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full0 + 8 * stage;
+                    mbar_expect_tx(fb, bytes);
+                    armed |= 1u << stage;
+                    armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                    const uint32_t a_dst = smem_u32(sA + stage * kABytes);
+                    const uint32_t b_dst = smem_u32(sB + stage * kBBytes);
+                    for (int i = 0; i < nbox; ++i)
+                        tma_load_2d(a_dst + i * kBoxRowsA * BKB, ta, fb, kb * BKB, a_y + i * kBoxRowsA);
+                    tma_load_2d(b_dst, &tm_b, fb, kb * BKB, b_y);
+                    if (EPI == EPI_SWIGLU) tma_load_2d(b_dst + 128 * BKB, &tm_b2, fb, kb * BKB, b_y);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                for (int s = 0; s < kStages; ++s)
+                    if (armed & (1u << s)) {
+                        volatile int never = 0;
+                        mbar_wait(full0 + 8 * s, (armed_parity >> s) & 1u, 1000000000LL, &never);
+                    }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ----------------------------------------------------- MMA issuer
+            int stage = 0;
+            uint32_t phase = 0, chunk = 0;
+            const uint32_t idesc = idesc_e4m3(BM, 256);
+            bool ok = true;
+            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    const uint32_t buf = chunk & 1u, cpar = (chunk >> 1) & 1u;
+                    if (!mbar_wait(full0 + 8 * stage, phase, lim, abort_flag) ||
+                        !mbar_wait(cempty0 + 8 * buf, cpar ^ 1u, lim, abort_flag)) {
+                        record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 12, blockIdx.x, u);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + buf * kAccCols;
+                    const uint64_t ad = umma_desc(smem_u32(sA + stage * kABytes));
+                    const uint64_t bd = umma_desc(smem_u32(sB + stage * kBBytes));
+#pragma unroll
+                    for (int kk = 0; kk < BKB / 32; ++kk)  // K=32 E4M3 per MMA: 32 bytes along the row
+                        umma_e4m3(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, kk != 0);
+                    umma_commit(empty0 + 8 * stage);
+                    umma_commit(cfull0 + 8 * buf);
+                    ++chunk;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            umma_commit(drain);
+            volatile int never = 0;
+            mbar_wait(drain, 0, 1000000000LL, &never);
+        }
+    }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
+        // ----------------------------------------------------------- epilogue
+        const int ew = warp - kEpiWarp0;
+        const int sub = warp & 3;      // TMEM lane quarter
+        const int half = ew >> 2;      // which half of the columns
+        const int row = sub * 32 + lane;
+        uint32_t chunk = 0, nunit = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++nunit) {
+            const int unit_par = nunit & 1;
+            const Unit un = decode_unit(p, u);
+            const bool sh = un.g == p.shared_group;
+            const int m = un.m0 + row;
+            const bool valid = m < un.nrows;
+            const int64_t arow = valid ? (sh ? (int64_t)m : (int64_t)un.row0 + m) : 0;
+            const float* asc = (sh ? p.a_shared_scale : p.a_scale) + arow * p.KB;
+            const int nblocks = p.N / 128;
+            float acc[128];
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            // weight scale rows for this unit: [g][block][KB]
+            const float* wsc1;
+            const float* wsc2;
+            if (EPI == EPI_SWIGLU) {
+                wsc1 = p.b_scale + ((int64_t)un.g * nblocks + un.nb) * p.KB;
+                wsc2 = p.b2_scale + ((int64_t)un.g * nblocks + un.nb) * p.KB;
+            } else {
+                wsc1 = p.b_scale + ((int64_t)un.g * nblocks + 2 * un.nb + half) * p.KB;
+                wsc2 = wsc1;
+            }
+            float sa_next = __ldg(asc), s1_next = __ldg(wsc1), s2_next = __ldg(wsc2);
+            for (int kb = 0; kb < p.KB; ++kb) {
+                const float sa = sa_next, s1 = s1_next, s2 = s2_next;
+                if (kb + 1 < p.KB) {  // next chunk's scales, fetched while this one is consumed
+                    sa_next = __ldg(asc + kb + 1);
+                    s1_next = __ldg(wsc1 + kb + 1);
+                    s2_next = __ldg(wsc2 + kb + 1);
+                }
+                const uint32_t buf = chunk & 1u, cpar = (chunk >> 1) & 1u;
+                int w_ok = 1;
+                if (lane == 0) {
+                    w_ok = mbar_wait(cfull0 + 8 * buf, cpar, lim, abort_flag);
+                    if (!w_ok) {
+                        record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 13, blockIdx.x, u);
+                        *abort_flag = 1;
+                    }
+                }
+                w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+                if (!w_ok) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tb = tmem_base + ((uint32_t)(sub * 32) << 16) + buf * kAccCols;
+                const float f1 = sa * s1, f2 = sa * s2;
+                if (EPI == EPI_SWIGLU) {
+                    // acc[0..63]: gate features 64*half.., acc[64..127]: up features
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t r[32];
+                        const int col = (q < 2) ? (64 * half + 32 * q) : (128 + 64 * half + 32 * (q - 2));
+                        tmem_ld32(tb + col, r);
+                        tmem_wait_ld();
+                        const float f = (q < 2) ? f1 : f2;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) acc[32 * q + i] = fmaf(__uint_as_float(r[i]), f, acc[32 * q + i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t r[32];
+                        tmem_ld32(tb + 128 * half + 32 * q, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) acc[32 * q + i] = fmaf(__uint_as_float(r[i]), f1, acc[32 * q + i]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cempty0 + 8 * buf);
+                ++chunk;
+            }
+            if (!ok) break;
+            const int64_t orow = (int64_t)un.row0 + m;
+            if (EPI == EPI_SWIGLU) {
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    acc[i] = swiglu(acc[i], acc[64 + i]);
+                    amax = fmaxf(amax, fabsf(acc[i]));
+                }
+                // the two column halves of a row meet in shared memory; an
+                // mbarrier (bounded wait) rather than a named barrier, so an
+                // aborting warp cannot strand the others
+                float* sm = s_amax + unit_par * 256;
+                sm[half * 128 + row] = amax;
+                const uint32_t xb = xbar0 + 8 * unit_par;
+                mbar_arrive(xb);
+                if (!mbar_wait(xb, (nunit >> 1) & 1u, lim, abort_flag)) {
+                    record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 14, blockIdx.x, u);
+                    *abort_flag = 1;
+                    break;
+                }
+                amax = fmaxf(sm[row], sm[128 + row]);
+                float sc = __fdiv_rn(amax, 448.0f), inv = __fdiv_rn(448.0f, amax);
+                if (amax == 0.0f) {
+                    sc = 1.0f;
+                    inv = 1.0f;
+                }
+                if (valid) {
+                    uint8_t* o = (uint8_t*)p.out + orow * p.ldo + un.nb * 128 + 64 * half;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const int i = 16 * v + 4 * j;
+                            w4[j] = (uint32_t)f32_to_e4m3(__fmul_rn(acc[i], inv)) |
+                                    ((uint32_t)f32_to_e4m3(__fmul_rn(acc[i + 1], inv)) << 8) |
+                                    ((uint32_t)f32_to_e4m3(__fmul_rn(acc[i + 2], inv)) << 16) |
+                                    ((uint32_t)f32_to_e4m3(__fmul_rn(acc[i + 3], inv)) << 24);
+                        }
+                        *(uint4*)(o + 16 * v) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                    if (half == 0) p.out_scale[orow * nblocks + un.nb] = sc;
+                }
+            } else if (valid) {
+                bf16* o = (bf16*)p.out + orow * p.ldo + un.nb * 256 + 128 * half;
+#pragma unroll
+                for (int v = 0; v < 16; ++v) {
+                    uint4 pk;
+                    __nv_bfloat162* h2 = (__nv_bfloat162*)&pk;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) h2[j] = __floats2bfloat162_rn(acc[8 * v + 2 * j], acc[8 * v + 2 * j + 1]);
+                    *(uint4*)(o + 8 * v) = pk;
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * kAccCols)
+                     : "memory");
+    }
+}
+
+bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+    auto fn = encode_fn();
+    if (!fn || rows < 1) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)cols};
+    cuuint32_t box[2] = {(cuuint32_t)BKB, (cuuint32_t)box_rows};
+    cuuint32_t es[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int EPI>
+cudaError_t launch_one(int grid, const CUtensorMap& ma, const CUtensorMap& msh, const CUtensorMap& mb,
+                       const CUtensorMap& mb2, const Params& p, cudaStream_t stream) {
+    static bool attr = false;
+    if (!attr) {
+        // The warpgroup register split (setmaxnreg) balances only at exactly
+        // kRegsLaunch registers per thread; anything else could leave the
+        // raising warpgroups waiting for registers that never come free.
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_fp8_kernel<EPI>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(gemm_fp8_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    gemm_fp8_kernel<EPI><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, p);
+    return cudaGetLastError();
+}
+
+}  // namespace f8
+}  // namespace tc
+
+bool gemm_fp8_supported(const GroupedGemm& g) {
+    using namespace tc::f8;
+    if (g.elem != kE4M3 || !g.offsets || !tc::encode_fn()) return false;
+    if (g.Ka != g.Kb || g.Kb % BKB || g.N % 128) return false;
+    if (!g.a_scale || !g.b_scale) return false;
+    if (g.b2) {
+        if (!g.b2_scale || !g.out_scale || g.out_elem != kE4M3 || !g.a_shared || !g.a_shared_scale) return false;
+    } else {
+        if (g.N % 256 || g.out_elem != kBF16) return false;
+    }
+    return true;
+}
+
+cudaError_t launch_gemm_fp8(const GroupedGemm& g, int num_sms, cudaStream_t stream) {
+    using namespace tc::f8;
+    const bool sw = g.b2 != nullptr;
+    Params p = {};
+    p.G = g.G;
+    p.shared_group = g.shared_group;
+    p.offsets = g.offsets;
+    p.tiles = g.tiles;
+    p.NB = sw ? g.N / 128 : g.N / 256;
+    p.N = g.N;
+    p.KB = g.Kb / BKB;
+    p.a_scale = g.a_scale;
+    p.a_shared_scale = g.a_shared_scale ? g.a_shared_scale : g.a_scale;
+    p.b_scale = g.b_scale;
+    p.b2_scale = g.b2_scale ? g.b2_scale : g.b_scale;
+    p.out = g.out;
+    p.ldo = g.ldo;
+    p.out_scale = g.out_scale;
+    p.err = g.err;
+    p.spin_ns = g.spin_ns > 0 ? g.spin_ns : 2000000000LL;
+    CUtensorMap ma, msh, mb, mb2;
+    if (!make_map_u8(&ma, g.a, g.a_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
+    if (g.a_shared) {
+        if (!make_map_u8(&msh, g.a_shared, g.a_shared_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
+    } else {
+        msh = ma;
+    }
+    if (!make_map_u8(&mb, g.b, (int64_t)g.G * g.N, g.Kb, sw ? 128 : 256)) return cudaErrorInvalidValue;
+    if (sw) {
+        if (!make_map_u8(&mb2, g.b2, (int64_t)g.G * g.N, g.Kb, 128)) return cudaErrorInvalidValue;
+    } else {
+        mb2 = mb;
+    }
+    const int max_units = g.max_tiles * p.NB;
+    if (max_units <= 0) return cudaGetLastError();
+    const int grid = std::max(1, std::min(num_sms, max_units));
+    cudaError_t e = sw ? launch_one<EPI_SWIGLU>(grid, ma, msh, mb, mb2, p, stream)
+                       : launch_one<EPI_PLAIN>(grid, ma, msh, mb, mb2, p, stream);
+    count_launches(1);
+    return e;
+}
+
+}  // namespace moe

@@ -9,7 +9,12 @@
 namespace moe {
 
 constexpr int kRowTile = 128;      // rows of the grouped layout per GEMM tile
-constexpr int kPermChunk = 1024;   // (t, j) pairs per permute chunk
+constexpr int kPermChunk = 1024;   // (t, j) pairs per permute chunk (largest size)
+
+// Pairs per permute chunk for T*k pairs: 128 up to 16384 pairs (more, shorter
+// chunks: the ranking walk is one warp per chunk), 1024 beyond (fewer
+// per-chunk histograms for the scan to walk).
+__host__ __device__ constexpr int perm_chunk(int64_t TK) { return TK <= 16384 ? 128 : kPermChunk; }
 
 // Element kinds of the GEMM operands.
 enum Elem : int { kF32 = 0, kBF16 = 1, kE4M3 = 2 };
@@ -61,6 +66,8 @@ void count_launches(int n);
 cudaError_t launch_gemm_simt(const GroupedGemm& g, cudaStream_t stream);
 cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t stream);
 bool gemm_tc_supported(const GroupedGemm& g);
+cudaError_t launch_gemm_fp8(const GroupedGemm& g, int num_sms, cudaStream_t stream);
+bool gemm_fp8_supported(const GroupedGemm& g);
 
 // Top-k over logits = sum_{s<S} part[s] (+ bias), summed in slice order;
 // when S > 1 or bias is given the summed logits are written to logits_out.

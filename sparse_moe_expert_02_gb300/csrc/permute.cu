@@ -7,7 +7,7 @@
 // Co-Design, and the Roofline").  The order inside each expert's segment is
 // the row-major (t, j) order of the pairs -- a stable counting sort -- so the
 // layout is deterministic and needs no atomics for positions:
-//   1. hist:   per chunk of kPermChunk pairs, a histogram over experts;
+//   1. hist:   per chunk of perm_chunk(T*k) pairs, a histogram over experts;
 //   2. scan:   per expert, an exclusive scan over chunks; then counts,
 //              offsets (with the shared expert's T rows appended) and the
 //              prefix of 128-row tiles the GEMMs walk;
@@ -27,10 +27,11 @@ namespace moe {
 __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restrict__ idx, int64_t TK, int E,
                                                         int32_t* __restrict__ hist, uint32_t* err) {
     extern __shared__ int32_t sh[];
+    const int chunk = perm_chunk(TK);
     for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
     __syncthreads();
-    const int64_t a0 = (int64_t)blockIdx.x * kPermChunk;
-    for (int i = threadIdx.x; i < kPermChunk; i += blockDim.x) {
+    const int64_t a0 = (int64_t)blockIdx.x * chunk;
+    for (int i = threadIdx.x; i < chunk; i += blockDim.x) {
         int64_t a = a0 + i;
         if (a < TK) {
             int e = __ldg(idx + a);
@@ -97,11 +98,12 @@ __global__ void __launch_bounds__(32) perm_rank_kernel(const int32_t* __restrict
                                                        int32_t* __restrict__ inv, int32_t* __restrict__ src_tok) {
     extern __shared__ int32_t cursor[];
     const int lane = threadIdx.x;
-    const int64_t a0 = (int64_t)blockIdx.x * kPermChunk;
+    const int chunk = perm_chunk(TK);
+    const int64_t a0 = (int64_t)blockIdx.x * chunk;
     for (int e = lane; e < E; e += 32) cursor[e] = __ldg(offsets + e) + __ldg(hist + (int64_t)blockIdx.x * E + e);
     __syncwarp();
     const unsigned lt = (1u << lane) - 1u;
-    for (int s = 0; s < kPermChunk; s += 32) {
+    for (int s = 0; s < chunk; s += 32) {
         const int64_t a = a0 + s + lane;
         const bool valid = a < TK;
         int e = valid ? __ldg(idx + a) : -1;
@@ -128,7 +130,7 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
                                  int32_t* offsets, int32_t* tiles, int32_t* inv, int32_t* src_tok, uint32_t* err,
                                  cudaStream_t stream) {
     const int64_t TK = (int64_t)T * k;
-    const int nch = (int)cdiv(TK, kPermChunk);
+    const int nch = (int)cdiv(TK, perm_chunk(TK));
     perm_hist_kernel<<<nch, 256, E * sizeof(int32_t), stream>>>(idx, TK, E, hist, err);
     perm_scan_kernel<<<1, 1024, 0, stream>>>(hist, nch, E, T, counts, offsets, tiles);
     perm_rank_kernel<<<nch, 32, E * sizeof(int32_t), stream>>>(idx, TK, k, E, hist, offsets, inv, src_tok);
@@ -290,7 +292,7 @@ extern "C" MOE_API moe_status moe_permute_index_noalloc(const int32_t* idx, int3
     if (!idx || !counts || !offsets || !tiles || !inv || !src_tok) return MOE_ERR_INVALID_ARG;
     if (T < 1 || E < 1 || E > 1024 || top_k < 1 || top_k > 32 || top_k > E) return MOE_ERR_INVALID_ARG;
     if ((int64_t)T * (top_k + 1) >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
-    const int64_t chunks = cdiv((int64_t)T * top_k, kPermChunk);
+    const int64_t chunks = cdiv((int64_t)T * top_k, perm_chunk((int64_t)T * top_k));
     if (chunks * E > kNoAllocHistInts) return MOE_ERR_UNSUPPORTED;  // beyond the static scratch
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return MOE_ERR_CUDA;

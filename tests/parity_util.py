@@ -37,8 +37,8 @@ def experts_for_tokens(idx: np.ndarray, weights: dict, mode: str, E: int):
         return t.index_select(0, groups.to(t.device)).cpu()
 
     if mode == "fp8":
-        ex = oracle.Experts("fp8", take("w_gate").numpy(), take("w_up").numpy(), take("w_down").numpy(),
-                            take("s_gate").numpy(), take("s_up").numpy(), take("s_down").numpy())
+        # fp32 originals, quantised by the oracle's own block codec
+        ex = oracle.Experts.quantised(take("w_gate"), take("w_up"), take("w_down"))
     else:
         ex = oracle.Experts(mode, take("w_gate"), take("w_up"), take("w_down"))
     return ex, idx_sub

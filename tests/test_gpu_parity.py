@@ -55,6 +55,10 @@ def _layer_parity(shape, inp, rows=None, flags=0, out_dtype="f32", check_y=True)
     if shape.dtype == "fp8":
         xq = v["xq"]
         assert torch.equal(v["xp"], xq[torch.as_tensor(src[:T * k], device="cuda").long()])
+        # activation quantisation is integer-deciding: bit-exact with the oracle's codec
+        q_o, s_o = oracle.quant_blocks(x.float().cpu().numpy(), 1, 128)
+        assert np.array_equal(xq.cpu().numpy(), q_o)
+        assert np.array_equal(v["xq_scale"].cpu().numpy(), s_o)
     else:
         assert torch.equal(v["xp"], x[torch.as_tensor(src[:T * k], device="cuda").long()])
     rows = np.arange(T) if rows is None else rows
@@ -63,7 +67,7 @@ def _layer_parity(shape, inp, rows=None, flags=0, out_dtype="f32", check_y=True)
     z_gpu = v["logits"][torch.as_tensor(rows, device="cuda")].double().cpu().numpy()
     assert np.abs(z_gpu - z_ref).max() <= 2e-4 * max(1.0, np.abs(z_ref).max())
     # layer output on the sampled rows, oracle routed by the GPU logits
-    ex, idx_sub = experts_for_tokens(idx[rows], layer.w, shape.dtype, E)
+    ex, idx_sub = experts_for_tokens(idx[rows], inp, shape.dtype, E)
     ref, y_ref = oracle.moe_tokens(x[rows].cpu(), idx_sub, w[rows], ex, want_y=True)
     got = out[torch.as_tensor(rows, device="cuda")].double().cpu().numpy()
     err = rel_max_err(got, ref)
@@ -248,6 +252,46 @@ def test_host_argument_errors():
     assert e.value.status == L.MOE_ERR_WORKSPACE
 
 
+# ------------------------------------------------------------- FP8 layer
+
+@pytest.mark.parametrize("T", [300, 1, 129])
+def test_small_fp8_layer(T):
+    shape = synth.SMALL_FP8.with_tokens(T)
+    _layer_parity(shape, _dev_inputs(shape, seed=9), out_dtype="bf16")
+
+
+def test_fp8_h_codes_mostly_match_oracle():
+    """h is quantised from fp32 accumulators on the GPU and from fp64 on the
+    oracle: codes agree except where h sits within rounding of a code
+    boundary, and the scales agree to within a few fp32 ulp."""
+    shape = synth.SMALL_FP8.with_tokens(64)
+    inp = _dev_inputs(shape, seed=10)
+    layer = MoELayer.from_shape(shape, inp, out_dtype="bf16")
+    layer.forward(inp["x"])
+    layer.check()
+    torch.cuda.synchronize()
+    v = layer.views(shape.T)
+    T, k, E = shape.T, shape.top_k, shape.E
+    idx, w = oracle.topk(v["logits"].double().cpu().numpy(), k)
+    inv = v["inv"].cpu().numpy()
+    ex = oracle.Experts.quantised(inp["w_gate"].cpu(), inp["w_up"].cpu(), inp["w_down"].cpu())
+    # oracle h of token 0's first expert, through the same codec
+    x0 = inp["x"][:1].float().cpu().numpy()
+    qx, sx = oracle.quant_blocks(x0, 1, 128)
+    xd = oracle.e4m3_decode(qx) * np.repeat(sx, 128, 1)
+    e = idx[0, 0]
+    deq = lambda q, s_: oracle.e4m3_decode(q) * np.repeat(np.repeat(s_, 128, 0), 128, 1)
+    a = xd @ deq(ex.wg[e], ex.sg[e]).T
+    u = xd @ deq(ex.wu[e], ex.su[e]).T
+    h = (a / (1 + np.exp(-a)) * u).astype(np.float32)
+    qh, sh = oracle.quant_blocks(h, 1, 128)
+    r = inv[0]
+    got_q = v["h"][r].cpu().numpy()
+    got_s = v["h_scale"][r].cpu().numpy()
+    assert np.mean(got_q == qh[0]) > 0.97
+    assert np.allclose(got_s, sh[0], rtol=1e-5)
+
+
 # ------------------------------------------------------ full-size workloads
 
 @pytest.fixture(scope="module")
@@ -269,3 +313,14 @@ def test_full_size_bf16_workloads(shape, big_bf16_weights):
         mean = shape.T * shape.top_k / shape.E
         assert counts.max() > 10 * mean, "the skewed workload must have straggler experts"
     assert torch.isfinite(out).all()
+
+
+def test_full_size_fp8_prefill():
+    shape = synth.PREFILL_FP8
+    inp = _dev_inputs(shape, seed=0)
+    rows = sample_rows(shape.T, 4, seed=2)
+    layer, out, err = _layer_parity(shape, inp, rows=rows, out_dtype="bf16", check_y=False)
+    counts = layer.views(shape.T)["counts"][:shape.E].cpu().numpy()
+    assert counts.max() > 10 * shape.T * shape.top_k / shape.E
+    del layer, inp
+    torch.cuda.empty_cache()
