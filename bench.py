@@ -159,7 +159,7 @@ def run_ours(args, shape, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     inp = synth.make_inputs(shape, seed=args.seed, device=dev)
-    layer = MoELayer.from_shape(shape, inp, device=local)
+    layer = MoELayer.from_shape(shape, inp, device=local, flags=args.flags)
     x = inp["x"]
     T = shape.T
     out = layer.new_out(T)
@@ -377,6 +377,7 @@ def main():
     ap.add_argument("--workload", default=synth.DECODE_BF16.name, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flags", type=int, default=0, help="moe_config.flags (kernel-path overrides)")
     ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample size for cpu_baseline")
     ap.add_argument("--experts", type=int, default=0,
                     help="override E (profiling captures on a few-GB copy of the workload); not a bench line")

@@ -91,6 +91,9 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2 } moe_
 
 /* moe_config.flags */
 #define MOE_FLAG_FORCE_SIMT 0x1u   /* expert GEMMs on the CUDA-core kernel (cross-check path) */
+#define MOE_FLAG_PAIR_CTA_OFF 0x2u /* bf16 expert GEMMs never on CTA pairs (cta_group::2) */
+#define MOE_FLAG_PAIR_CTA_ON 0x4u  /* bf16 expert GEMMs on CTA pairs at any T (default: when
+                                      T*top_k >= 128*E, i.e. prefill-sized groups) */
 
 typedef struct moe_config {
     int32_t T_max;           /* largest token count a call may pass */
@@ -140,6 +143,7 @@ typedef struct moe_ws_layout {
     size_t h_scale;    /* FP8: f32 [T*top_k + T, I/128] */
     size_t y;          /* [R, D] expert outputs: f32 (MOE_F32, MOE_BF16) or bf16 (FP8 layer) */
     size_t logits_part;/* f32 [S, T, E] router K-slice partials when T is small (S > 1), else 0 */
+    size_t tiles2;     /* int32 [E+2]: exclusive prefix of ceil(counts/256) (row-tile pairs) */
 } moe_ws_layout;
 
 /* Validate a configuration and build a host-side plan for `device`.

@@ -25,6 +25,8 @@ MOE_ERR_CUDA, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_BOUNDS, MOE_ERR_NONFINITE = 4, 5, 
 # moe_dtype
 MOE_F32, MOE_BF16, MOE_FP8_E4M3_B128 = 0, 1, 2
 MOE_FLAG_FORCE_SIMT = 0x1
+MOE_FLAG_PAIR_CTA_OFF = 0x2
+MOE_FLAG_PAIR_CTA_ON = 0x4
 
 DTYPE_CODE = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8": MOE_FP8_E4M3_B128}
 
@@ -52,7 +54,7 @@ class moe_weights(ctypes.Structure):
 class moe_ws_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("total", "err", "logits", "blob", "counts", "offsets", "tiles", "inv", "src_tok", "hist", "xq",
-                 "xq_scale", "xp", "xp_scale", "h", "h_scale", "y", "logits_part")]
+                 "xq_scale", "xp", "xp_scale", "h", "h_scale", "y", "logits_part", "tiles2")]
 
 
 class MoEError(RuntimeError):

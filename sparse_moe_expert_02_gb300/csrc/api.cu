@@ -82,6 +82,7 @@ void layout(const moe_config& c, int num_sms, int T, moe_ws_layout* L) {
     L->y = take((size_t)R * c.D * (c.dtype == MOE_FP8_E4M3_B128 ? 2 : 4));
     const int S = route_splits(c, T, num_sms);
     L->logits_part = S > 1 ? take((size_t)S * T * c.E * 4) : 0;
+    L->tiles2 = take((size_t)(c.E + 2) * 4);
     L->total = o;
 }
 
@@ -135,13 +136,27 @@ moe_status run_gemm(const moe_plan* p, const moe::GroupedGemm& g, cudaStream_t s
         return MOE_OK;
     }
     if (use_tc(p, g)) {
-        MOE_CUDA(moe::launch_gemm_tc(g, p->num_sms, s));
+        if (g.prefer_pairs && moe::gemm_tc2_supported(g)) MOE_CUDA(moe::launch_gemm_tc2(g, p->num_sms, s));
+        else MOE_CUDA(moe::launch_gemm_tc(g, p->num_sms, s));
         return MOE_OK;
     }
     if (g.elem == moe::kE4M3) return arg_fail(MOE_ERR_UNSUPPORTED, "FP8 GEMM shape without a tensor-core kernel");
     cudaError_t e = moe::launch_gemm_simt(g, s);
     if (e != cudaSuccess) return cuda_fail(e, what);
     return MOE_OK;
+}
+
+// CTA pairs pay off once the routed groups hold a few hundred rows on
+// average (prefill); decode-sized groups stay on single CTAs.
+int prefer_pairs(const moe_plan* p, int T) {
+    if (p->cfg.flags & MOE_FLAG_PAIR_CTA_OFF) return 0;
+    if (p->cfg.flags & MOE_FLAG_PAIR_CTA_ON) return 1;
+    return (int64_t)T * p->cfg.top_k >= (int64_t)128 * p->cfg.E;
+}
+
+int grouped_max_tiles2(const moe_config& c, int T) {
+    const int64_t R = (int64_t)T * (c.top_k + 1);
+    return (int)(R / (2 * moe::kRowTile) + c.E + 2);
 }
 
 int grouped_max_tiles(const moe_config& c, int T) {
@@ -303,7 +318,8 @@ moe_status moe_permute(const moe_plan* p, const void* x, int32_t T, void* ws, si
     const int TK = T * c.top_k;
     MOE_CUDA(moe::launch_permute_index(W.at<int32_t>(W.L.blob), T, c.E, c.top_k, W.at<int32_t>(W.L.hist),
                                        W.at<int32_t>(W.L.counts), W.at<int32_t>(W.L.offsets),
-                                       W.at<int32_t>(W.L.tiles), W.at<int32_t>(W.L.inv), W.at<int32_t>(W.L.src_tok),
+                                       W.at<int32_t>(W.L.tiles), W.at<int32_t>(W.L.tiles2), W.at<int32_t>(W.L.inv),
+                                       W.at<int32_t>(W.L.src_tok),
                                        W.at<uint32_t>(W.L.err), s));
     if (c.dtype == MOE_FP8_E4M3_B128) {
         MOE_CUDA(moe::launch_quant_rows(x, moe::kBF16, T, c.D, W.at<uint8_t>(W.L.xq), W.at<float>(W.L.xq_scale), s));
@@ -334,6 +350,9 @@ moe_status moe_gemm_gateup(const moe_plan* p, const moe_weights* w, const void* 
     g.offsets = W.at<int32_t>(W.L.offsets);
     g.tiles = W.at<int32_t>(W.L.tiles);
     g.max_tiles = grouped_max_tiles(c, T);
+    g.tiles2 = W.at<int32_t>(W.L.tiles2);
+    g.max_tiles2 = grouped_max_tiles2(c, T);
+    g.prefer_pairs = prefer_pairs(p, T);
     g.N = c.I;
     g.Ka = g.Kb = c.D;
     g.out_pair = c.dtype == MOE_BF16;
@@ -371,6 +390,9 @@ moe_status moe_gemm_down(const moe_plan* p, const moe_weights* w, int32_t T, voi
     g.offsets = W.at<int32_t>(W.L.offsets);
     g.tiles = W.at<int32_t>(W.L.tiles);
     g.max_tiles = grouped_max_tiles(c, T);
+    g.tiles2 = W.at<int32_t>(W.L.tiles2);
+    g.max_tiles2 = grouped_max_tiles2(c, T);
+    g.prefer_pairs = prefer_pairs(p, T);
     g.N = c.D;
     g.Kb = c.I;
     g.Ka = (c.dtype == MOE_BF16) ? 2 * c.I : c.I;  // hi/lo pair walks W_down twice

@@ -30,6 +30,9 @@ struct GroupedGemm {
     int shared_group;            // group whose A rows come from a_shared (-1: none)
     const int32_t* offsets;      // [G+1] device (nullptr: single group of `rows` rows)
     const int32_t* tiles;        // [G+1] device prefix of ceil(rows/128) (nullptr with offsets)
+    const int32_t* tiles2;       // [G+1] device prefix of ceil(rows/256), or nullptr
+    int max_tiles2;              // host bound on the total number of 256-row tiles
+    int prefer_pairs;            // 1: run on CTA pairs (M=256) when a kernel for it exists
     int rows;                    // single-group row count
     int max_tiles;               // host bound on the total number of row tiles
     int N;                       // output columns (features) of one group
@@ -66,6 +69,8 @@ void count_launches(int n);
 cudaError_t launch_gemm_simt(const GroupedGemm& g, cudaStream_t stream);
 cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t stream);
 bool gemm_tc_supported(const GroupedGemm& g);
+cudaError_t launch_gemm_tc2(const GroupedGemm& g, int num_sms, cudaStream_t stream);
+bool gemm_tc2_supported(const GroupedGemm& g);
 cudaError_t launch_gemm_fp8(const GroupedGemm& g, int num_sms, cudaStream_t stream);
 bool gemm_fp8_supported(const GroupedGemm& g);
 
@@ -75,9 +80,11 @@ cudaError_t launch_topk(const float* part, int S, const float* bias, float* logi
                         int32_t* blob, uint32_t* err, cudaStream_t stream);
 int router_splits(int T, int E, int D, int num_sms);
 
+// tiles2 (nullable): exclusive prefix of ceil(counts/256), the row-tile
+// pairs of the two-CTA GEMM.
 cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_t* hist, int32_t* counts,
-                                 int32_t* offsets, int32_t* tiles, int32_t* inv, int32_t* src_tok, uint32_t* err,
-                                 cudaStream_t stream);
+                                 int32_t* offsets, int32_t* tiles, int32_t* tiles2, int32_t* inv, int32_t* src_tok,
+                                 uint32_t* err, cudaStream_t stream);
 cudaError_t launch_gather_rows(const void* x, int elem_bytes, int64_t row_bytes, const int32_t* src_tok,
                                int rows, void* xp, cudaStream_t stream);
 cudaError_t launch_quant_rows(const void* x, int x_elem, int rows, int cols, uint8_t* q, float* s,

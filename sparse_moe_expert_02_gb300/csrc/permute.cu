@@ -66,9 +66,10 @@ __device__ void warp_exclusive_scan(const int32_t* v, int n, int32_t* out) {
 
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E, int T,
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                                                         int32_t* __restrict__ tiles) {
+                                                         int32_t* __restrict__ tiles, int32_t* __restrict__ tiles2) {
     __shared__ int32_t cnt[1025 + 1];
     __shared__ int32_t ntile[1025 + 1];
+    __shared__ int32_t ntile2[1025 + 1];
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         int run = 0;
         for (int c = 0; c < nchunks; ++c) {
@@ -79,15 +80,18 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ h
         }
         cnt[e] = run;
         ntile[e] = (run + kRowTile - 1) / kRowTile;
+        ntile2[e] = (run + 2 * kRowTile - 1) / (2 * kRowTile);
     }
     if (threadIdx.x == 0) {
         cnt[E] = T;
         ntile[E] = (T + kRowTile - 1) / kRowTile;
+        ntile2[E] = (T + 2 * kRowTile - 1) / (2 * kRowTile);
     }
     __syncthreads();
     for (int e = threadIdx.x; e <= E; e += blockDim.x) counts[e] = cnt[e];
     if (threadIdx.x < 32) warp_exclusive_scan(cnt, E + 1, offsets);
     else if (threadIdx.x < 64) warp_exclusive_scan(ntile, E + 1, tiles);
+    else if (threadIdx.x < 96 && tiles2) warp_exclusive_scan(ntile2, E + 1, tiles2);
 }
 
 // ------------------------------------------------------------------ rank
@@ -127,12 +131,12 @@ __global__ void shared_rows_kernel(int32_t* __restrict__ src_tok, int64_t TK, in
 }
 
 cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_t* hist, int32_t* counts,
-                                 int32_t* offsets, int32_t* tiles, int32_t* inv, int32_t* src_tok, uint32_t* err,
-                                 cudaStream_t stream) {
+                                 int32_t* offsets, int32_t* tiles, int32_t* tiles2, int32_t* inv, int32_t* src_tok,
+                                 uint32_t* err, cudaStream_t stream) {
     const int64_t TK = (int64_t)T * k;
     const int nch = (int)cdiv(TK, perm_chunk(TK));
     perm_hist_kernel<<<nch, 256, E * sizeof(int32_t), stream>>>(idx, TK, E, hist, err);
-    perm_scan_kernel<<<1, 1024, 0, stream>>>(hist, nch, E, T, counts, offsets, tiles);
+    perm_scan_kernel<<<1, 1024, 0, stream>>>(hist, nch, E, T, counts, offsets, tiles, tiles2);
     perm_rank_kernel<<<nch, 32, E * sizeof(int32_t), stream>>>(idx, TK, k, E, hist, offsets, inv, src_tok);
     shared_rows_kernel<<<(unsigned)cdiv(T, 256), 256, 0, stream>>>(src_tok, TK, T);
     count_launches(4);
@@ -311,7 +315,7 @@ extern "C" MOE_API moe_status moe_permute_index_noalloc(const int32_t* idx, int3
     // Every histogram entry a chunk uses is written by the hist kernel before
     // the scan reads it, so what an earlier call left in the array is never
     // read and nothing needs clearing.
-    if (launch_permute_index(idx, T, E, top_k, hist, counts, offsets, tiles, inv, src_tok, nullptr,
+    if (launch_permute_index(idx, T, E, top_k, hist, counts, offsets, tiles, nullptr, inv, src_tok, nullptr,
                              (cudaStream_t)stream) != cudaSuccess)
         return MOE_ERR_CUDA;
     return MOE_OK;

@@ -99,8 +99,9 @@ def test_small_fp32_ragged(T):
     _layer_parity(shape, _dev_inputs(shape, seed=3))
 
 
-@pytest.mark.parametrize("flags", [0, L.MOE_FLAG_FORCE_SIMT], ids=["default", "simt"])
-@pytest.mark.parametrize("T", [300, 1, 128, 129])
+@pytest.mark.parametrize("flags", [0, L.MOE_FLAG_FORCE_SIMT, L.MOE_FLAG_PAIR_CTA_ON],
+                         ids=["default", "simt", "cta_pairs"])
+@pytest.mark.parametrize("T", [300, 1, 128, 129, 700])
 def test_small_bf16_layer(flags, T):
     shape = synth.SMALL_BF16.with_tokens(T)
     _layer_parity(shape, _dev_inputs(shape, seed=4), flags=flags)
@@ -301,13 +302,14 @@ def big_bf16_weights():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("shape", [synth.DECODE_BF16, synth.BATCHED_DECODE_BF16, synth.PREFILL_BF16],
-                         ids=lambda s: s.name)
-def test_full_size_bf16_workloads(shape, big_bf16_weights):
+@pytest.mark.parametrize("shape,flags", [(synth.DECODE_BF16, 0), (synth.BATCHED_DECODE_BF16, 0),
+                                         (synth.PREFILL_BF16, 0), (synth.PREFILL_BF16, L.MOE_FLAG_PAIR_CTA_OFF)],
+                         ids=["decode", "batched_decode", "prefill_cta_pairs", "prefill_single_cta"])
+def test_full_size_bf16_workloads(shape, flags, big_bf16_weights):
     inp = _dev_inputs(shape, seed=0, weights=False)
     inp.update(big_bf16_weights)
     rows = sample_rows(shape.T, 6, seed=1)
-    layer, out, _ = _layer_parity(shape, inp, rows=rows, check_y=False)
+    layer, out, _ = _layer_parity(shape, inp, rows=rows, check_y=False, flags=flags)
     if shape.zipf_s is not None and shape.T >= 8192:
         counts = layer.views(shape.T)["counts"][:shape.E].cpu().numpy()
         mean = shape.T * shape.top_k / shape.E
