@@ -96,6 +96,7 @@ template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_sh,
                     const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
+                    const __grid_constant__ CUtensorMap tm_af, const __grid_constant__ CUtensorMap tm_a_shf,
                     const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -153,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Unit un = decode_unit(p, u);
                 const bool sh = un.g == p.shared_group;
                 const CUtensorMap* ta = sh ? &tm_a_sh : &tm_a;
+                const CUtensorMap* taf = sh ? &tm_a_shf : &tm_af;
                 const int a_y = sh ? un.m0 : un.row0 + un.m0;
                 const int valid = min(BM, un.nrows - un.m0);
                 const int nbox = (valid + kBoxRowsA - 1) / kBoxRowsA;
@@ -171,8 +173,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     const uint32_t a_dst = smem_u32(sA + stage * kABytes);
                     const uint32_t b_dst = smem_u32(sB + stage * kBBytes);
-                    for (int i = 0; i < nbox; ++i)
-                        tma_load_2d(a_dst + i * kBoxRowsA * BKB, ta, fb, kb * BKB, a_y + i * kBoxRowsA);
+                    if (nbox * kBoxRowsA == BM) {  // (nearly) full tile: one 128-row box
+                        tma_load_2d(a_dst, taf, fb, kb * BKB, a_y);
+                    } else {
+                        for (int i = 0; i < nbox; ++i)
+                            tma_load_2d(a_dst + i * kBoxRowsA * BKB, ta, fb, kb * BKB, a_y + i * kBoxRowsA);
+                    }
                     tma_load_2d(b_dst, &tm_b, fb, kb * BKB, b_y);
                     if (EPI == EPI_SWIGLU) tma_load_2d(b_dst + 128 * BKB, &tm_b2, fb, kb * BKB, b_y);
                     if (++stage == kStages) {
@@ -392,7 +398,8 @@ bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, i
 
 template <int EPI>
 cudaError_t launch_one(int grid, const CUtensorMap& ma, const CUtensorMap& msh, const CUtensorMap& mb,
-                       const CUtensorMap& mb2, const Params& p, cudaStream_t stream) {
+                       const CUtensorMap& mb2, const CUtensorMap& maf, const CUtensorMap& mshf, const Params& p,
+                       cudaStream_t stream) {
     static bool attr = false;
     if (!attr) {
         // The warpgroup register split (setmaxnreg) balances only at exactly
@@ -406,7 +413,7 @@ cudaError_t launch_one(int grid, const CUtensorMap& ma, const CUtensorMap& msh, 
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    gemm_fp8_kernel<EPI><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, p);
+    gemm_fp8_kernel<EPI><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, maf, mshf, p);
     return cudaGetLastError();
 }
 
@@ -446,12 +453,15 @@ cudaError_t launch_gemm_fp8(const GroupedGemm& g, int num_sms, cudaStream_t stre
     p.out_scale = g.out_scale;
     p.err = g.err;
     p.spin_ns = g.spin_ns > 0 ? g.spin_ns : 2000000000LL;
-    CUtensorMap ma, msh, mb, mb2;
+    CUtensorMap ma, msh, mb, mb2, maf, mshf;
     if (!make_map_u8(&ma, g.a, g.a_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
+    if (!make_map_u8(&maf, g.a, g.a_rows, g.Ka, BM)) return cudaErrorInvalidValue;
     if (g.a_shared) {
         if (!make_map_u8(&msh, g.a_shared, g.a_shared_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
+        if (!make_map_u8(&mshf, g.a_shared, g.a_shared_rows, g.Ka, BM)) return cudaErrorInvalidValue;
     } else {
         msh = ma;
+        mshf = maf;
     }
     if (!make_map_u8(&mb, g.b, (int64_t)g.G * g.N, g.Kb, sw ? 128 : 256)) return cudaErrorInvalidValue;
     if (sw) {
@@ -462,8 +472,8 @@ cudaError_t launch_gemm_fp8(const GroupedGemm& g, int num_sms, cudaStream_t stre
     const int max_units = g.max_tiles * p.NB;
     if (max_units <= 0) return cudaGetLastError();
     const int grid = std::max(1, std::min(num_sms, max_units));
-    cudaError_t e = sw ? launch_one<EPI_SWIGLU>(grid, ma, msh, mb, mb2, p, stream)
-                       : launch_one<EPI_PLAIN>(grid, ma, msh, mb, mb2, p, stream);
+    cudaError_t e = sw ? launch_one<EPI_SWIGLU>(grid, ma, msh, mb, mb2, maf, mshf, p, stream)
+                       : launch_one<EPI_PLAIN>(grid, ma, msh, mb, mb2, maf, mshf, p, stream);
     count_launches(1);
     return e;
 }

@@ -44,7 +44,9 @@ constexpr int kABytes = BM * BK * 2;      // 16 KB: one A tile
 constexpr int kBBytesMax = 256 * BK * 2;  // 32 KB
 constexpr int kThreads = 192;
 constexpr int kAccCols = 256;             // TMEM columns per accumulator buffer
-constexpr int kBoxRowsA = 16;             // A is fetched in 16-row boxes (2 KB)
+constexpr int kBoxRowsA = 16;             // a ragged tile's A rows come in 16-row boxes (2 KB);
+                                          // a full tile's in one 128-row box: the single
+                                          // producer thread issues few TMA instructions
 constexpr uint32_t kSmemBytes = 1024 + 196608 + 256;
 
 // Stage geometry.  PAIR: A is a bf16 hi/lo pair (hi in columns [0, Kb), lo in
@@ -125,6 +127,7 @@ template <int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_sh,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
+                   const __grid_constant__ CUtensorMap tm_af, const __grid_constant__ CUtensorMap tm_a_shf,
                    const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -180,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Unit un = decode_unit(p, u, total_tiles);
                 const bool sh = un.g == p.shared_group;
                 const CUtensorMap* ta = sh ? &tm_a_sh : &tm_a;
+                const CUtensorMap* taf = sh ? &tm_a_shf : &tm_af;
                 const int a_y = sh ? un.m0 : un.row0 + un.m0;
                 const int valid = min(BM, un.nrows - un.m0);
                 const int nbox = (valid + kBoxRowsA - 1) / kBoxRowsA;
@@ -198,11 +202,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     const uint32_t a_dst = smem_u32(sA + stage * kAStage);
                     const uint32_t b_dst = smem_u32(sB + stage * kBBytesMax);
-                    for (int i = 0; i < nbox; ++i) {
-                        tma_load_2d(a_dst + i * kBoxRowsA * 128, ta, fb, kb * BK, a_y + i * kBoxRowsA);
-                        if (PAIR)
-                            tma_load_2d(a_dst + kABytes + i * kBoxRowsA * 128, ta, fb, p.a_lo_x + kb * BK,
-                                        a_y + i * kBoxRowsA);
+                    if (nbox * kBoxRowsA == BM) {  // (nearly) full tile: one 128-row box
+                        tma_load_2d(a_dst, taf, fb, kb * BK, a_y);
+                        if (PAIR) tma_load_2d(a_dst + kABytes, taf, fb, p.a_lo_x + kb * BK, a_y);
+                    } else {
+                        for (int i = 0; i < nbox; ++i) {
+                            tma_load_2d(a_dst + i * kBoxRowsA * 128, ta, fb, kb * BK, a_y + i * kBoxRowsA);
+                            if (PAIR)
+                                tma_load_2d(a_dst + kABytes + i * kBoxRowsA * 128, ta, fb, p.a_lo_x + kb * BK,
+                                            a_y + i * kBoxRowsA);
+                        }
                     }
                     const int bx = kb * BK;
                     tma_load_2d(b_dst, &tm_b, fb, bx, b_y);
@@ -408,7 +417,8 @@ int plain_bn(int N) {
 
 template <int EPI, bool PAIR>
 cudaError_t launch_one(int grid, const CUtensorMap& ma, const CUtensorMap& msh, const CUtensorMap& mb,
-                       const CUtensorMap& mb2, const Params& p, cudaStream_t stream) {
+                       const CUtensorMap& mb2, const CUtensorMap& maf, const CUtensorMap& mshf, const Params& p,
+                       cudaStream_t stream) {
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -416,7 +426,7 @@ cudaError_t launch_one(int grid, const CUtensorMap& ma, const CUtensorMap& msh, 
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    gemm_tc_kernel<EPI, PAIR><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, p);
+    gemm_tc_kernel<EPI, PAIR><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, maf, mshf, p);
     return cudaGetLastError();
 }
 
@@ -476,13 +486,16 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     p.err = g.err;
     p.spin_ns = g.spin_ns > 0 ? g.spin_ns : 2000000000LL;
 
-    CUtensorMap ma, msh, mb, mb2;
+    CUtensorMap ma, msh, mb, mb2, maf, mshf;
     const int G = g.offsets ? g.G : 1;
     if (!make_map(&ma, g.a, g.a_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
+    if (!make_map(&maf, g.a, g.a_rows, g.Ka, BM)) return cudaErrorInvalidValue;
     if (g.a_shared) {
         if (!make_map(&msh, g.a_shared, g.a_shared_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
+        if (!make_map(&mshf, g.a_shared, g.a_shared_rows, g.Ka, BM)) return cudaErrorInvalidValue;
     } else {
         msh = ma;
+        mshf = maf;
     }
     const int brow_box = sw ? 128 : p.BN;
     if (!make_map(&mb, g.b, (int64_t)G * g.N, g.Kb, brow_box)) return cudaErrorInvalidValue;
@@ -495,9 +508,9 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     if (max_units <= 0) return cudaGetLastError();
     const int grid = std::max(1, std::min(num_sms, max_units));
     cudaError_t e;
-    if (sw) e = launch_one<EPI_SWIGLU, false>(grid, ma, msh, mb, mb2, p, stream);
-    else if (pair) e = launch_one<EPI_PLAIN, true>(grid, ma, msh, mb, mb2, p, stream);
-    else e = launch_one<EPI_PLAIN, false>(grid, ma, msh, mb, mb2, p, stream);
+    if (sw) e = launch_one<EPI_SWIGLU, false>(grid, ma, msh, mb, mb2, maf, mshf, p, stream);
+    else if (pair) e = launch_one<EPI_PLAIN, true>(grid, ma, msh, mb, mb2, maf, mshf, p, stream);
+    else e = launch_one<EPI_PLAIN, false>(grid, ma, msh, mb, mb2, maf, mshf, p, stream);
     count_launches(1);
     return e;
 }

@@ -94,6 +94,7 @@ template <int EPI, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc2_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_sh,
                     const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
+                    const __grid_constant__ CUtensorMap tm_af, const __grid_constant__ CUtensorMap tm_a_shf,
                     const Params p) {
     constexpr int kStages = Geo<PAIR>::kStages;
     constexpr int kAStage = Geo<PAIR>::kAStage;
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Unit un = decode_unit(p, u);
                 const bool sh = un.g == p.shared_group;
                 const CUtensorMap* ta = sh ? &tm_a_sh : &tm_a;
+                const CUtensorMap* taf = sh ? &tm_a_shf : &tm_af;
                 const int m0 = un.m0pair + (int)rank * BM;
                 const int nbox = boxes_for(un.nrows, m0);
                 const int a_y = sh ? m0 : un.row0 + m0;
@@ -166,11 +168,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (leader) mbar_expect_tx(fb_local, pair_bytes);
                     const uint32_t a_dst = smem_u32(sA + stage * kAStage);
                     const uint32_t b_dst = smem_u32(sB + stage * kBHalf);
-                    for (int i = 0; i < nbox; ++i) {
-                        tma_load_2d_pair(a_dst + i * kBoxRowsA * 128, ta, fb, kb * BK, a_y + i * kBoxRowsA);
-                        if (PAIR)
-                            tma_load_2d_pair(a_dst + kABytes + i * kBoxRowsA * 128, ta, fb, p.a_lo_x + kb * BK,
-                                             a_y + i * kBoxRowsA);
+                    if (nbox * kBoxRowsA == BM) {  // full half-tile: one 128-row box
+                        tma_load_2d_pair(a_dst, taf, fb, kb * BK, a_y);
+                        if (PAIR) tma_load_2d_pair(a_dst + kABytes, taf, fb, p.a_lo_x + kb * BK, a_y);
+                    } else {
+                        for (int i = 0; i < nbox; ++i) {
+                            tma_load_2d_pair(a_dst + i * kBoxRowsA * 128, ta, fb, kb * BK, a_y + i * kBoxRowsA);
+                            if (PAIR)
+                                tma_load_2d_pair(a_dst + kABytes + i * kBoxRowsA * 128, ta, fb,
+                                                 p.a_lo_x + kb * BK, a_y + i * kBoxRowsA);
+                        }
                     }
                     tma_load_2d_pair(b_dst, tb, fb, kb * BK, b_y);
                     if (++stage == kStages) {
@@ -321,7 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int EPI, bool PAIR>
 cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& msh, const CUtensorMap& mb, const CUtensorMap& mb2,
-                       const Params& p, int max_units, int num_sms, cudaStream_t stream) {
+                       const CUtensorMap& maf, const CUtensorMap& mshf, const Params& p, int max_units, int num_sms,
+                       cudaStream_t stream) {
     auto kern = gemm_tc2_kernel<EPI, PAIR>;
     static int max_clusters = 0;
     if (max_clusters == 0) {
@@ -356,7 +364,7 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& msh, const CUte
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ma, msh, mb, mb2, p);
+    return cudaLaunchKernelEx(&cfg, kern, ma, msh, mb, mb2, maf, mshf, p);
 }
 
 }  // namespace p2
@@ -387,12 +395,15 @@ cudaError_t launch_gemm_tc2(const GroupedGemm& g, int num_sms, cudaStream_t stre
     p.out = g.out;
     p.err = g.err;
     p.spin_ns = g.spin_ns > 0 ? g.spin_ns : 2000000000LL;
-    CUtensorMap ma, msh, mb, mb2;
+    CUtensorMap ma, msh, mb, mb2, maf, mshf;
     if (!tc::make_map(&ma, g.a, g.a_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
+    if (!tc::make_map(&maf, g.a, g.a_rows, g.Ka, BM)) return cudaErrorInvalidValue;
     if (g.a_shared) {
         if (!tc::make_map(&msh, g.a_shared, g.a_shared_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
+        if (!tc::make_map(&mshf, g.a_shared, g.a_shared_rows, g.Ka, BM)) return cudaErrorInvalidValue;
     } else {
         msh = ma;
+        mshf = maf;
     }
     if (!tc::make_map(&mb, g.b, (int64_t)g.G * g.N, g.Kb, 128)) return cudaErrorInvalidValue;
     if (sw) {
@@ -403,9 +414,9 @@ cudaError_t launch_gemm_tc2(const GroupedGemm& g, int num_sms, cudaStream_t stre
     const int max_units = g.max_tiles2 * p.NB;
     if (max_units <= 0) return cudaGetLastError();
     cudaError_t e;
-    if (sw) e = launch_one<EPI_SWIGLU, false>(ma, msh, mb, mb2, p, max_units, num_sms, stream);
-    else if (pair) e = launch_one<EPI_PLAIN, true>(ma, msh, mb, mb2, p, max_units, num_sms, stream);
-    else e = launch_one<EPI_PLAIN, false>(ma, msh, mb, mb2, p, max_units, num_sms, stream);
+    if (sw) e = launch_one<EPI_SWIGLU, false>(ma, msh, mb, mb2, maf, mshf, p, max_units, num_sms, stream);
+    else if (pair) e = launch_one<EPI_PLAIN, true>(ma, msh, mb, mb2, maf, mshf, p, max_units, num_sms, stream);
+    else e = launch_one<EPI_PLAIN, false>(ma, msh, mb, mb2, maf, mshf, p, max_units, num_sms, stream);
     count_launches(1);
     return e;
 }
