@@ -91,9 +91,8 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2 } moe_
 
 /* moe_config.flags */
 #define MOE_FLAG_FORCE_SIMT 0x1u   /* expert GEMMs on the CUDA-core kernel (cross-check path) */
-#define MOE_FLAG_PAIR_CTA_OFF 0x2u /* bf16 expert GEMMs never on CTA pairs (cta_group::2) */
-#define MOE_FLAG_PAIR_CTA_ON 0x4u  /* bf16 expert GEMMs on CTA pairs at any T (default: when
-                                      T*top_k >= 128*E, i.e. prefill-sized groups) */
+#define MOE_FLAG_PAIR_CTA_OFF 0x2u /* bf16 expert GEMMs never on CTA pairs (the default) */
+#define MOE_FLAG_PAIR_CTA_ON 0x4u  /* bf16 expert GEMMs on CTA pairs (cta_group::2, 256-row tiles) */
 
 typedef struct moe_config {
     int32_t T_max;           /* largest token count a call may pass */

@@ -303,8 +303,8 @@ def big_bf16_weights():
 
 
 @pytest.mark.parametrize("shape,flags", [(synth.DECODE_BF16, 0), (synth.BATCHED_DECODE_BF16, 0),
-                                         (synth.PREFILL_BF16, 0), (synth.PREFILL_BF16, L.MOE_FLAG_PAIR_CTA_OFF)],
-                         ids=["decode", "batched_decode", "prefill_cta_pairs", "prefill_single_cta"])
+                                         (synth.PREFILL_BF16, 0), (synth.PREFILL_BF16, L.MOE_FLAG_PAIR_CTA_ON)],
+                         ids=["decode", "batched_decode", "prefill", "prefill_cta_pairs"])
 def test_full_size_bf16_workloads(shape, flags, big_bf16_weights):
     inp = _dev_inputs(shape, seed=0, weights=False)
     inp.update(big_bf16_weights)
