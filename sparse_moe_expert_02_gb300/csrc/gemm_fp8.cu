@@ -106,8 +106,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
     const uint32_t cfull0 = smem_u32(bars + 2 * kStages), cempty0 = smem_u32(bars + 2 * kStages + 2);
     const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
-    const uint32_t xbar0 = smem_u32(bars + 2 * kStages + 5);  // [2]: amax exchange, one per unit parity
-    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kStages + 7);
+    // [2 unit parities][4 lane quarters]: amax exchange between the two warps
+    // that hold the two column halves of the same 32 rows
+    const uint32_t xbar0 = smem_u32(bars + 2 * kStages + 5);
+    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kStages + 13);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
     float* s_amax = (float*)(smem + kStages * (kABytes + kBBytes) + 256);  // [2 units][2 halves][128 rows]
 
@@ -122,8 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(cempty0 + 8 * b, kEpiWarps);
         }
         mbar_init(drain, 1);
-        mbar_init(xbar0, kEpiWarps * 32);
-        mbar_init(xbar0 + 8, kEpiWarps * 32);
+        for (int b = 0; b < 8; ++b) mbar_init(xbar0 + 8 * b, 2 * 32);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -289,26 +290,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t tb = tmem_base + ((uint32_t)(sub * 32) << 16) + buf * kAccCols;
                 const float f1 = sa * s1, f2 = sa * s2;
-                if (EPI == EPI_SWIGLU) {
-                    // acc[0..63]: gate features 64*half.., acc[64..127]: up features
+                // Two 32-column TMEM loads per wait, then the promotion with
+                // paired fp32 FMAs (two lanes of work per instruction).
+                // SwiGLU: q=0 -> gate columns 64*half.., q=1 -> up columns
+                // 128+64*half..; plain: q -> columns 128*half + 64*q.
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t r[32];
-                        const int col = (q < 2) ? (64 * half + 32 * q) : (128 + 64 * half + 32 * (q - 2));
-                        tmem_ld32(tb + col, r);
-                        tmem_wait_ld();
-                        const float f = (q < 2) ? f1 : f2;
+                for (int q = 0; q < 2; ++q) {
+                    uint32_t r[64];
+                    const int col = (EPI == EPI_SWIGLU) ? (q == 0 ? 64 * half : 128 + 64 * half) : 128 * half + 64 * q;
+                    tmem_ld32x2(tb + col, r);
+                    tmem_wait_ld();
+                    const float f = (EPI == EPI_SWIGLU && q == 1) ? f2 : f1;
+                    const float2 ff = make_float2(f, f);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[32 * q + i] = fmaf(__uint_as_float(r[i]), f, acc[32 * q + i]);
-                    }
-                } else {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        uint32_t r[32];
-                        tmem_ld32(tb + 128 * half + 32 * q, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) acc[32 * q + i] = fmaf(__uint_as_float(r[i]), f1, acc[32 * q + i]);
+                    for (int i = 0; i < 64; i += 2) {
+                        float2 a = make_float2(acc[64 * q + i], acc[64 * q + i + 1]);
+                        a = __ffma2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), ff, a);
+                        acc[64 * q + i] = a.x;
+                        acc[64 * q + i + 1] = a.y;
                     }
                 }
                 tc_fence_before();
@@ -330,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // aborting warp cannot strand the others
                 float* sm = s_amax + unit_par * 256;
                 sm[half * 128 + row] = amax;
-                const uint32_t xb = xbar0 + 8 * unit_par;
+                const uint32_t xb = xbar0 + 8 * (unit_par * 4 + sub);
                 mbar_arrive(xb);
                 if (!mbar_wait(xb, (nunit >> 1) & 1u, lim, abort_flag)) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 14, blockIdx.x, u);
