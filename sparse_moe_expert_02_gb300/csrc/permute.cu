@@ -126,6 +126,87 @@ __global__ void __launch_bounds__(32) perm_rank_kernel(const int32_t* __restrict
     }
 }
 
+// ------------------------------------------------- small problems, one block
+//
+// The same stable counting sort for T*k <= kSmallPairs pairs in one launch of
+// one 1024-thread block, everything in shared memory: warp w owns the w-th
+// 32nd of the pairs (histogram, then its ranks), thread e scans expert e over
+// the 32 warps.  Decode-sized routing (1280 pairs) spends ~5 us here instead
+// of four dependent launches.
+constexpr int kSmallPairs = 8192;
+constexpr int kSmallMaxE = 512;
+constexpr int kSmallSmem = (32 * kSmallMaxE + 4 * (kSmallMaxE + 2)) * 4;
+
+__global__ void __launch_bounds__(1024) perm_index_small_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
+                                                                int32_t* __restrict__ counts,
+                                                                int32_t* __restrict__ offsets,
+                                                                int32_t* __restrict__ tiles,
+                                                                int32_t* __restrict__ tiles2, int32_t* __restrict__ inv,
+                                                                int32_t* __restrict__ src_tok, uint32_t* err) {
+    extern __shared__ int32_t sm[];
+    int32_t* hist = sm;                   // [32][E]: per-warp counts, then cursors
+    int32_t* cnt = hist + 32 * E;         // [E+1]
+    int32_t* nt = cnt + (E + 2);          // [E+1] 128-row tiles
+    int32_t* nt2 = nt + (E + 2);          // [E+1] 256-row tiles
+    int32_t* off = nt2 + (E + 2);         // [E+2]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int TK = T * k;
+    const int per = (TK + 31) / 32;
+    const int a0 = warp * per, a1 = min(TK, a0 + per);
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int a = a0 + lane; a < a1; a += 32) {
+        const int e = __ldg(idx + a);
+        if ((unsigned)e < (unsigned)E) atomicAdd(&hist[warp * E + e], 1);
+        else record_error(err, MOE_ERR_BOUNDS, (uint32_t)a, (uint32_t)e, 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+#pragma unroll 8
+        for (int w = 0; w < 32; ++w) {
+            const int v = hist[w * E + e];
+            hist[w * E + e] = run;
+            run += v;
+        }
+        cnt[e] = run;
+        nt[e] = (run + kRowTile - 1) / kRowTile;
+        nt2[e] = (run + 2 * kRowTile - 1) / (2 * kRowTile);
+    }
+    if (threadIdx.x == 0) {
+        cnt[E] = T;
+        nt[E] = (T + kRowTile - 1) / kRowTile;
+        nt2[E] = (T + 2 * kRowTile - 1) / (2 * kRowTile);
+    }
+    __syncthreads();
+    if (warp == 0) warp_exclusive_scan(cnt, E + 1, off);
+    else if (warp == 1) warp_exclusive_scan(nt, E + 1, tiles);
+    else if (warp == 2 && tiles2) warp_exclusive_scan(nt2, E + 1, tiles2);
+    __syncthreads();
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) counts[e] = cnt[e];
+    for (int e = threadIdx.x; e <= E + 1; e += blockDim.x) offsets[e] = off[e];
+    for (int i = threadIdx.x; i < 32 * E; i += blockDim.x) hist[i] += off[i % E];  // cursors
+    for (int t = threadIdx.x; t < T; t += blockDim.x) src_tok[TK + t] = t;
+    __syncthreads();
+    const unsigned lt = (1u << lane) - 1u;
+    int32_t* cur = hist + warp * E;
+    for (int s = a0; s < a1; s += 32) {
+        const int a = s + lane;
+        int e = (a < a1) ? __ldg(idx + a) : -1;
+        if ((unsigned)e >= (unsigned)E) e = -1;
+        const unsigned peers = __match_any_sync(0xffffffffu, e);
+        int pos = 0;
+        if (e >= 0) pos = cur[e] + __popc(peers & lt);
+        __syncwarp();
+        if (e >= 0 && (peers >> lane) == 1u) cur[e] += __popc(peers);
+        __syncwarp();
+        if (e >= 0) {
+            inv[a] = pos;
+            src_tok[pos] = a / k;
+        }
+    }
+}
+
 __global__ void shared_rows_kernel(int32_t* __restrict__ src_tok, int64_t TK, int T) {
     for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) src_tok[TK + t] = t;
 }
@@ -134,6 +215,20 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
                                  int32_t* offsets, int32_t* tiles, int32_t* tiles2, int32_t* inv, int32_t* src_tok,
                                  uint32_t* err, cudaStream_t stream) {
     const int64_t TK = (int64_t)T * k;
+    if (TK <= kSmallPairs && E <= kSmallMaxE) {
+        static bool attr = false;
+        if (!attr) {
+            cudaError_t e = cudaFuncSetAttribute(perm_index_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kSmallSmem);
+            if (e != cudaSuccess) return e;
+            attr = true;
+        }
+        const int smem = (32 * E + 4 * (E + 2)) * 4;
+        perm_index_small_kernel<<<1, 1024, smem, stream>>>(idx, T, E, k, counts, offsets, tiles, tiles2, inv, src_tok,
+                                                           err);
+        count_launches(1);
+        return cudaGetLastError();
+    }
     const int nch = (int)cdiv(TK, perm_chunk(TK));
     perm_hist_kernel<<<nch, 256, E * sizeof(int32_t), stream>>>(idx, TK, E, hist, err);
     perm_scan_kernel<<<1, 1024, 0, stream>>>(hist, nch, E, T, counts, offsets, tiles, tiles2);

@@ -29,19 +29,25 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
     const float* zt = part + (int64_t)t * E;
     float v[J];
     bool finite = true;
+    // K-split partial products of the router GEMM, added in slice order; the
+    // loads of one slice are independent, so each slice costs one round trip
+#pragma unroll
+    for (int j = 0; j < J; ++j) v[j] = (lane + 32 * j < E) ? __ldg(zt + lane + 32 * j) : 0.0f;
+    for (int s = 1; s < S; ++s) {
+        float w[J];
+#pragma unroll
+        for (int j = 0; j < J; ++j) w[j] = (lane + 32 * j < E) ? __ldg(zt + s * TE + lane + 32 * j) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < J; ++j) v[j] += w[j];
+    }
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const int e = lane + 32 * j;
-        float z = 0.0f;
         if (e < E) {
-            // K-split partial products of the router GEMM, added in slice order
-            z = __ldg(zt + e);
-            for (int s = 1; s < S; ++s) z += __ldg(zt + s * TE + e);
-            if (bias) z += __ldg(bias + e);
-            if (logits_out) logits_out[(int64_t)t * E + e] = z;
+            if (bias) v[j] += __ldg(bias + e);
+            if (logits_out) logits_out[(int64_t)t * E + e] = v[j];
+            if (!isfinite(v[j])) finite = false;
         }
-        v[j] = z;
-        if (e < E && !isfinite(z)) finite = false;
     }
     if (!__all_sync(0xffffffffu, finite)) {
         if (lane == 0) record_error(err, MOE_ERR_NONFINITE, (uint32_t)t, 0, 0);

@@ -16,13 +16,16 @@
 
 namespace moe {
 
+// grid = (T, ceil(D / (blockDim*V))): one 16-byte vector of one token per
+// thread.  The k+1 source rows are read in groups of 8 independent loads, so
+// a token costs two round trips to memory instead of k+1.
 template <typename TY, typename TO>
 __global__ void __launch_bounds__(256) unpermute_kernel(const TY* __restrict__ y, const int32_t* __restrict__ blob,
                                                         const int32_t* __restrict__ inv, int T, int D, int k,
                                                         TO* __restrict__ out, uint32_t* err) {
     constexpr int V = 16 / sizeof(TY);  // elements per 16-byte vector of y
     __shared__ int64_t rows[33];
-    __shared__ float wts[32];
+    __shared__ float wts[33];
     const int t = blockIdx.x;
     const int64_t TK = (int64_t)T * k;
     if (threadIdx.x < k) {
@@ -33,46 +36,53 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const TY* __restrict__ y
             r = 0;
             wj = 0.0f;
         }
-        rows[threadIdx.x] = (int64_t)r * D;
-        wts[threadIdx.x] = wj;
+        rows[1 + threadIdx.x] = (int64_t)r * D;
+        wts[1 + threadIdx.x] = wj;
     }
-    if (threadIdx.x == 0) rows[32] = (TK + t) * D;
+    if (threadIdx.x == 0) {  // slot 0: the shared expert's row, weight 1
+        rows[0] = (TK + t) * D;
+        wts[0] = 1.0f;
+    }
     __syncthreads();
-    for (int c = threadIdx.x * V; c < D; c += blockDim.x * V) {
-        float acc[V];
-        {
-            const int4 v = __ldg((const int4*)(y + rows[32] + c));
-            const TY* e = (const TY*)&v;
+    const int c = (blockIdx.y * blockDim.x + threadIdx.x) * V;
+    if (c >= D) return;
+    float acc[V];
 #pragma unroll
-            for (int i = 0; i < V; ++i) acc[i] = to_f32(e[i]);
-        }
-        for (int j = 0; j < k; ++j) {
-            const int4 v = __ldg((const int4*)(y + rows[j] + c));
-            const TY* e = (const TY*)&v;
-            const float wj = wts[j];
+    for (int i = 0; i < V; ++i) acc[i] = 0.0f;
+    // slot order: shared expert first, then j = 0 .. k-1 (fp32 accumulation)
+    for (int j0 = 0; j0 <= k; j0 += 8) {
+        int4 v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (j0 + q <= k) v[q] = __ldg((const int4*)(y + rows[j0 + q] + c));
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            if (j0 + q > k) break;
+            const TY* e = (const TY*)&v[q];
+            const float wj = wts[j0 + q];
 #pragma unroll
             for (int i = 0; i < V; ++i) acc[i] = fmaf(wj, to_f32(e[i]), acc[i]);
         }
-        // This thread owns out[t, c .. c+V-1]: V*sizeof(TO) bytes at a
-        // multiple of that size (16 B for fp32 out, 8 or 16 B for bf16 out).
-        TO* o = out + (int64_t)t * D + c;
-        if constexpr (sizeof(TO) == 4) {
+    }
+    // This thread owns out[t, c .. c+V-1]: V*sizeof(TO) bytes at a
+    // multiple of that size (16 B for fp32 out, 8 or 16 B for bf16 out).
+    TO* o = out + (int64_t)t * D + c;
+    if constexpr (sizeof(TO) == 4) {
 #pragma unroll
-            for (int i = 0; i < V; i += 4) *(float4*)(o + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-        } else if constexpr (V == 4) {
-            uint2 p;
-            __nv_bfloat162* pb = (__nv_bfloat162*)&p;
-            pb[0] = __floats2bfloat162_rn(acc[0], acc[1]);
-            pb[1] = __floats2bfloat162_rn(acc[2], acc[3]);
-            *(uint2*)o = p;
-        } else {
-            static_assert(V == 8, "bf16 y carries 8 values per 16-byte vector");
-            uint4 p;
-            __nv_bfloat162* pb = (__nv_bfloat162*)&p;
+        for (int i = 0; i < V; i += 4) *(float4*)(o + i) = make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+    } else if constexpr (V == 4) {
+        uint2 p;
+        __nv_bfloat162* pb = (__nv_bfloat162*)&p;
+        pb[0] = __floats2bfloat162_rn(acc[0], acc[1]);
+        pb[1] = __floats2bfloat162_rn(acc[2], acc[3]);
+        *(uint2*)o = p;
+    } else {
+        static_assert(V == 8, "bf16 y carries 8 values per 16-byte vector");
+        uint4 p;
+        __nv_bfloat162* pb = (__nv_bfloat162*)&p;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) pb[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-            *(uint4*)o = p;
-        }
+        for (int q = 0; q < 4; ++q) pb[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+        *(uint4*)o = p;
     }
 }
 
@@ -80,15 +90,17 @@ cudaError_t launch_unpermute(const void* y, int y_elem, const int32_t* blob, con
                              void* out, int out_elem, uint32_t* err, cudaStream_t stream) {
     if (T <= 0) return cudaGetLastError();
     const int V = (y_elem == kF32) ? 4 : 8;
-    int threads = (int)std::min<int64_t>(256, ((D / V + 31) / 32) * 32);
+    const int vecs = D / V;
+    const int threads = std::min(256, ((vecs + 31) / 32) * 32);
+    dim3 grid((unsigned)T, (unsigned)cdiv(vecs, threads));
     if (y_elem == kF32 && out_elem == kF32)
-        unpermute_kernel<float, float><<<T, threads, 0, stream>>>((const float*)y, blob, inv, T, D, k, (float*)out, err);
+        unpermute_kernel<float, float><<<grid, threads, 0, stream>>>((const float*)y, blob, inv, T, D, k, (float*)out, err);
     else if (y_elem == kF32)
-        unpermute_kernel<float, bf16><<<T, threads, 0, stream>>>((const float*)y, blob, inv, T, D, k, (bf16*)out, err);
+        unpermute_kernel<float, bf16><<<grid, threads, 0, stream>>>((const float*)y, blob, inv, T, D, k, (bf16*)out, err);
     else if (out_elem == kF32)
-        unpermute_kernel<bf16, float><<<T, threads, 0, stream>>>((const bf16*)y, blob, inv, T, D, k, (float*)out, err);
+        unpermute_kernel<bf16, float><<<grid, threads, 0, stream>>>((const bf16*)y, blob, inv, T, D, k, (float*)out, err);
     else
-        unpermute_kernel<bf16, bf16><<<T, threads, 0, stream>>>((const bf16*)y, blob, inv, T, D, k, (bf16*)out, err);
+        unpermute_kernel<bf16, bf16><<<grid, threads, 0, stream>>>((const bf16*)y, blob, inv, T, D, k, (bf16*)out, err);
     count_launches(1);
     return cudaGetLastError();
 }
