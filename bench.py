@@ -374,7 +374,8 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=synth.DECODE_BF16.name, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default=synth.DECODE_BF16.name,
+                    choices=sorted(synth.WORKLOADS) + sorted(synth.EXTRA_WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flags", type=int, default=0, help="moe_config.flags (kernel-path overrides)")
@@ -385,7 +386,7 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    shape = synth.WORKLOADS[args.workload]
+    shape = {**synth.WORKLOADS, **synth.EXTRA_WORKLOADS}[args.workload]
     if args.experts:
         import dataclasses
         shape = dataclasses.replace(shape, E=args.experts, name=f"{shape.name}_E{args.experts}_profile")

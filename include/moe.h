@@ -229,6 +229,15 @@ MOE_API moe_status moe_permute_index_noalloc(const int32_t* idx, int32_t T, int3
                                              int32_t* counts, int32_t* offsets, int32_t* tiles, int32_t* inv,
                                              int32_t* src_tok, void* stream);
 
+/* Compact routing word (English page, "Fusing Three Collectives Into Two":
+ * indices and weights packed into one dense 32-bit blob).  From the
+ * workspace blob of the last moe_route / moe_forward for T tokens, writes
+ * words [T, top_k] int32: bits 0..15 the expert index, bits 16..31 the bf16
+ * (round to nearest even) of the fp32 routing weight.  Half the bytes of the
+ * two-plane blob; the weight keeps 8 significant bits. */
+MOE_API moe_status moe_pack_routing_words(const moe_plan* plan, int32_t T, const void* ws, size_t ws_bytes,
+                                          int32_t* words, void* stream);
+
 /* Synchronise `stream`, read the workspace error word and return the first
  * device-side error recorded since the last clear (MOE_OK if none). */
 MOE_API moe_status moe_check(const moe_plan* plan, const void* ws, void* stream);

@@ -75,6 +75,7 @@ def lib():
             L.orc_moe_tokens.argtypes = [I64, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P]
             L.orc_moe_layer.argtypes = [I64, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P]
             L.orc_pack_blob.argtypes = [I64, I32, P, P, P]
+            L.orc_pack_words.argtypes = [I64, I32, P, P, P]
             L.orc_unpermute.argtypes = [I64, I32, I32, P, P, P, P]
             _lib = L
     return _lib
@@ -176,6 +177,16 @@ def pack_blob(idx: np.ndarray, w: np.ndarray) -> np.ndarray:
     blob = np.empty((2, T, k), np.int32)
     lib().orc_pack_blob(T, k, _p(idx), _p(w32), _p(blob))
     return blob
+
+
+def pack_words(idx: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """One int32 per slot: index in bits 0..15, bf16 weight in bits 16..31."""
+    idx = _c(idx, np.int32)
+    w32 = _c(w, np.float32)
+    T, k = idx.shape
+    out = np.empty((T, k), np.int32)
+    lib().orc_pack_words(T, k, _p(idx), _p(w32), _p(out))
+    return out
 
 
 def unpermute(y: np.ndarray, w: np.ndarray, inv: np.ndarray, T: int, k: int) -> np.ndarray:

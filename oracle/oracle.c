@@ -351,6 +351,15 @@ ORC_EXPORT void orc_pack_blob(int64_t T, int32_t k, const int32_t* idx, const fl
     }
 }
 
+/* Compact one-word form of the same blob: bits 0..15 the expert index,
+ * bits 16..31 the bf16 (round to nearest even) of the fp32 weight. */
+ORC_EXPORT void orc_pack_words(int64_t T, int32_t k, const int32_t* idx, const float* w, int32_t* words) {
+    for (int64_t i = 0; i < T * k; ++i) {
+        uint32_t word = ((uint32_t)idx[i] & 0xFFFFu) | ((uint32_t)orc_f32_to_bf16(w[i]) << 16);
+        memcpy(&words[i], &word, 4);
+    }
+}
+
 /* Combine step on its own (unpermute): out[t] = y[T*k + t] + sum_j w[t,j] *
  * y[inv[t*k+j]], over rows y of the expert-contiguous layout, in double. */
 ORC_EXPORT void orc_unpermute(int64_t T, int32_t D, int32_t k, const double* y, const double* w,

@@ -36,7 +36,7 @@ SYMBOLS = (
     "moe_workspace_init", "moe_quantize_weights", "moe_forward", "moe_route", "moe_topk", "moe_permute",
     "moe_gemm_gateup", "moe_gemm_down", "moe_unpermute", "moe_check", "moe_selftest_wait_timeout",
     "moe_status_str", "moe_last_error_detail", "moe_build_info", "moe_launch_count",
-    "moe_permute_index_noalloc",
+    "moe_permute_index_noalloc", "moe_pack_routing_words",
 )
 
 
@@ -101,6 +101,7 @@ def lib():
                 "moe_build_info": (ctypes.c_char_p, []),
                 "moe_launch_count": (ctypes.c_uint64, []),
                 "moe_permute_index_noalloc": (st, [P, I32, I32, I32, P, P, P, P, P, P]),
+                "moe_pack_routing_words": (st, [P, I32, P, S, P, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -227,6 +228,11 @@ def moe_permute_index_noalloc(idx, T, E, top_k, counts, offsets, tiles, inv, src
     """Allocation-free permutation index build; returns the moe_status."""
     return lib().moe_permute_index_noalloc(_ptr(idx), T, E, top_k, _ptr(counts), _ptr(offsets), _ptr(tiles),
                                            _ptr(inv), _ptr(src_tok), _stream(stream))
+
+
+def moe_pack_routing_words(plan, T, ws, words, stream=None):
+    _ok(lib().moe_pack_routing_words(plan, T, _ptr(ws), _wsb(ws), _ptr(words), _stream(stream)),
+        "moe_pack_routing_words")
 
 
 def moe_launch_count() -> int:

@@ -450,6 +450,16 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
     return MOE_OK;
 }
 
+moe_status moe_pack_routing_words(const moe_plan* p, int32_t T, const void* ws, size_t ws_bytes, int32_t* words,
+                                  void* stream) {
+    Ws W;
+    moe_status st = check_call(p, T, const_cast<void*>(ws), ws_bytes, &W);
+    if (st != MOE_OK) return st;
+    if (!ptr_ok(words)) return arg_fail(MOE_ERR_INVALID_ARG, "words NULL or misaligned");
+    MOE_CUDA(moe::launch_pack_words(W.at<int32_t>(W.L.blob), (int64_t)T * p->cfg.top_k, words, (cudaStream_t)stream));
+    return MOE_OK;
+}
+
 moe_status moe_check(const moe_plan* p, const void* ws, void* stream) {
     if (!p || !ws) return arg_fail(MOE_ERR_INVALID_ARG, "NULL argument");
     uint32_t word[4] = {0, 0, 0, 0};

@@ -79,6 +79,7 @@ bool gemm_fp8_supported(const GroupedGemm& g);
 cudaError_t launch_topk(const float* part, int S, const float* bias, float* logits_out, int T, int E, int k,
                         int32_t* blob, uint32_t* err, cudaStream_t stream);
 int router_splits(int T, int E, int D, int num_sms);
+cudaError_t launch_pack_words(const int32_t* blob, int64_t TK, int32_t* words, cudaStream_t stream);
 
 // tiles2 (nullable): exclusive prefix of ceil(counts/256), the row-tile
 // pairs of the two-CTA GEMM.

@@ -110,6 +110,26 @@ cudaError_t launch_topk(const float* part, int S, const float* bias, float* logi
     return cudaGetLastError();
 }
 
+// Compact routing word: one int32 per (t, j) holding the expert index in the
+// low 16 bits and the bf16 (round to nearest even) of the routing weight in
+// the high 16 -- the single dense 32-bit blob of the English page's
+// "Fusing Three Collectives Into Two", at half the bytes of the two-plane
+// blob (the weight keeps 8 significant bits).
+__global__ void pack_words_kernel(const int32_t* __restrict__ blob, int64_t TK, int32_t* __restrict__ words) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < TK; i += (int64_t)gridDim.x * blockDim.x) {
+        const uint32_t e = (uint32_t)__ldg(blob + i) & 0xFFFFu;
+        const uint32_t w = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(__int_as_float(__ldg(blob + TK + i))));
+        words[i] = (int32_t)(e | (w << 16));
+    }
+}
+
+cudaError_t launch_pack_words(const int32_t* blob, int64_t TK, int32_t* words, cudaStream_t stream) {
+    const int blocks = (int)std::min<int64_t>(cdiv(TK, 256), 4096);
+    pack_words_kernel<<<blocks, 256, 0, stream>>>(blob, TK, words);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 // K slices of the router GEMM: enough (up to 8) that the units of 32
 // experts x 128 tokens x K/S cover the SMs when T is small.
 int router_splits(int T, int E, int D, int num_sms) {

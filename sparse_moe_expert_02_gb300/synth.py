@@ -64,6 +64,12 @@ PREFILL_FP8 = LayerShape("prefill_fp8_T16384_zipf1.2", 16384, 4096, 512, 1024, 1
 
 WORKLOADS = {s.name: s for s in (TINY_F32, DECODE_BF16, BATCHED_DECODE_BF16, PREFILL_BF16, PREFILL_FP8)}
 
+# FP8 weights at the decode shapes: the memory-bound regime streams half the
+# bytes (E4M3 codes + 128x128 block scales instead of bf16).
+DECODE_FP8 = LayerShape("decode_fp8_T128_D4096_E512_I1024_k10", 128, 4096, 512, 1024, 10, "fp8")
+BATCHED_DECODE_FP8 = LayerShape("batched_decode_fp8_T1024_zipf1.0", 1024, 4096, 512, 1024, 10, "fp8", 1.0)
+EXTRA_WORKLOADS = {s.name: s for s in (DECODE_FP8, BATCHED_DECODE_FP8)}
+
 # Reduced shapes for parity tests: several tiles in every dimension plus a
 # ragged tail, small enough for the oracle to finish in seconds.
 SMALL_BF16 = LayerShape("small_bf16_T300_D512_E32_I256_k4_zipf1.2", 300, 512, 32, 256, 4, "bf16", 1.2)

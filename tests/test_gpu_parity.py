@@ -134,6 +134,20 @@ def test_forward_outputs_blob_and_logits():
     assert np.array_equal(blob[0].cpu().numpy(), idx)
 
 
+def test_compact_routing_words_bit_exact():
+    shape = synth.SMALL_BF16
+    inp = _dev_inputs(shape, seed=11)
+    layer = MoELayer.from_shape(shape, inp)
+    layer.forward(inp["x"])
+    T, k = shape.T, shape.top_k
+    words = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    L.moe_pack_routing_words(layer.plan, T, layer.ws, words)
+    torch.cuda.synchronize()
+    blob = layer.views(T)["blob"].cpu().numpy()
+    ref = oracle.pack_words(blob[0], blob[1].view(np.float32))
+    assert np.array_equal(words.cpu().numpy(), ref)
+
+
 # ------------------------------------------------------------- stage tests
 
 @pytest.mark.parametrize("T,E,k", [(300, 16, 2), (1000, 512, 10), (37, 1000, 32), (5, 7, 7)])
@@ -324,5 +338,15 @@ def test_full_size_fp8_prefill():
     layer, out, err = _layer_parity(shape, inp, rows=rows, out_dtype="bf16", check_y=False)
     counts = layer.views(shape.T)["counts"][:shape.E].cpu().numpy()
     assert counts.max() > 10 * shape.T * shape.top_k / shape.E
+    del layer, inp
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("shape", [synth.DECODE_FP8, synth.BATCHED_DECODE_FP8], ids=lambda s: s.name)
+def test_full_size_fp8_decode(shape):
+    """FP8 weights at the decode shapes (half the streamed bytes)."""
+    inp = _dev_inputs(shape, seed=0)
+    rows = sample_rows(shape.T, 4, seed=3)
+    layer, out, err = _layer_parity(shape, inp, rows=rows, out_dtype="bf16", check_y=False)
     del layer, inp
     torch.cuda.empty_cache()

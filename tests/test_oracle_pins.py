@@ -142,6 +142,20 @@ def test_blob_round_trip():
     assert np.array_equal(blob[1].view(np.float32), w.astype(np.float32))
 
 
+def test_compact_word_matches_independent_packing():
+    """One-word blob: low 16 bits the index, high 16 bits bf16(w); checked
+    against numpy bit twiddling over torch's bf16 rounding."""
+    g = np.random.default_rng(8)
+    idx, w = oracle.topk(g.normal(size=(500, 512)), 10)
+    words = oracle.pack_words(idx, w).view(np.uint32)
+    wb = torch.from_numpy(w.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ref = (idx.astype(np.uint32) & 0xFFFF) | (wb.astype(np.uint32) << 16)
+    assert np.array_equal(words, ref)
+    assert np.array_equal((words & 0xFFFF).astype(np.int32), idx)
+    back = (words >> 16).astype(np.uint32) << 16
+    assert np.allclose(back.view(np.float32), w, rtol=2.0 ** -8, atol=0)
+
+
 # ------------------------------------------------------------ permutation
 
 @pytest.mark.parametrize("T,E,k,seed", [(64, 16, 2, 0), (300, 32, 4, 1), (7, 5, 5, 2), (1, 3, 1, 3)])
