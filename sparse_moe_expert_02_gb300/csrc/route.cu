@@ -18,28 +18,47 @@
 
 namespace moe {
 
-template <int J>  // J = ceil(E / 32) logits per lane
+// Order-preserving map of an fp32 to uint32 (larger float -> larger key);
+// -0 is folded onto +0 first so that the two compare equal, as floats do.
+__device__ __forceinline__ uint32_t order_key(float v) {
+    if (v == 0.0f) v = 0.0f;
+    const uint32_t u = __float_as_uint(v);
+    return (u >> 31) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+    return __uint_as_float((k >> 31) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+template <int J>  // J = ceil(E / 32) logits per lane, a power of two
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int S,
                                                    const float* __restrict__ bias, float* __restrict__ logits_out,
                                                    int T, int E, int k, int32_t* __restrict__ blob, uint32_t* err) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (t >= T) return;
+    if (t >= T) return;  // whole warps leave together
     const int64_t TE = (int64_t)T * E;
     const float* zt = part + (int64_t)t * E;
+    // K-split partial products of the router GEMM (S slices): the loads of a
+    // batch of SB slices are all issued before the first add, and the slices
+    // are added in order
+    constexpr int SB = (J <= 16) ? 8 : 2;
     float v[J];
-    bool finite = true;
-    // K-split partial products of the router GEMM, added in slice order; the
-    // loads of one slice are independent, so each slice costs one round trip
 #pragma unroll
-    for (int j = 0; j < J; ++j) v[j] = (lane + 32 * j < E) ? __ldg(zt + lane + 32 * j) : 0.0f;
-    for (int s = 1; s < S; ++s) {
-        float w[J];
+    for (int j = 0; j < J; ++j) v[j] = 0.0f;
+    for (int s0 = 0; s0 < S; s0 += SB) {
+        float w[SB][J];
 #pragma unroll
-        for (int j = 0; j < J; ++j) w[j] = (lane + 32 * j < E) ? __ldg(zt + s * TE + lane + 32 * j) : 0.0f;
+        for (int s = 0; s < SB; ++s)
 #pragma unroll
-        for (int j = 0; j < J; ++j) v[j] += w[j];
+            for (int j = 0; j < J; ++j)
+                w[s][j] = (s0 + s < S && lane + 32 * j < E) ? __ldg(zt + (s0 + s) * TE + lane + 32 * j) : 0.0f;
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+#pragma unroll
+            for (int s = 0; s < SB; ++s)
+                if (s0 + s < S) v[j] = (s0 + s == 0) ? w[s][j] : v[j] + w[s][j];
     }
+    bool finite = true;
 #pragma unroll
     for (int j = 0; j < J; ++j) {
         const int e = lane + 32 * j;
@@ -57,29 +76,52 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
         for (int j = 0; j < J; ++j)
             if (!isfinite(v[j])) v[j] = -INFINITY;
     }
-    uint32_t taken = 0;  // bit j: this lane's slot j is chosen
-    float zsel = 0.0f;   // lane r < k keeps the r-th chosen logit
+    // Each lane sorts its logits once: larger first, lower expert index first
+    // among equals (the lane's experts are lane, lane+32, ...).  Key 0 marks
+    // an empty slot: every real logit (even -inf) has a larger key.
+    uint32_t key[J];
+    int id[J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        key[j] = (e < E) ? order_key(v[j]) : 0u;
+        id[j] = e;
+    }
+#pragma unroll
+    for (int size = 2; size <= J; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < J; ++i) {
+                const int l = i ^ stride;
+                if (l > i) {
+                    const bool first_up = (i & size) == 0;  // keep the better one at i
+                    const bool l_better = key[l] > key[i] || (key[l] == key[i] && id[l] < id[i]);
+                    if (l_better == first_up) {
+                        const uint32_t tk = key[i]; key[i] = key[l]; key[l] = tk;
+                        const int ti = id[i]; id[i] = id[l]; id[l] = ti;
+                    }
+                }
+            }
+    // k rounds: the largest head over the warp, the lowest index among the
+    // lanes holding it; that lane drops its head.
+    float zsel = 0.0f;
     int isel = 0;
     for (int r = 0; r < k; ++r) {
-        float bv = 0.0f;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-            int e = lane + 32 * j;
-            bool ok = (e < E) && !((taken >> j) & 1u);
-            // lanes scan j upwards, so e grows: strict '>' keeps the lowest e on ties
-            if (ok && (bi == 0x7fffffff || v[j] > bv)) { bv = v[j]; bi = e; }
+        const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
+        const uint32_t win = __reduce_min_sync(0xffffffffu, key[0] == m ? (uint32_t)id[0] : 0xFFFFFFFFu);
+        if (lane == r) {
+            zsel = key_value(m);
+            isel = (int)win;
         }
+        if (key[0] == m && (uint32_t)id[0] == win) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            bool take = (oi != 0x7fffffff) &&
-                        (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi));
-            if (take) { bv = ov; bi = oi; }
+            for (int j = 0; j + 1 < J; ++j) {
+                key[j] = key[j + 1];
+                id[j] = id[j + 1];
+            }
+            key[J - 1] = 0u;
         }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == r) { zsel = bv; isel = bi; }
     }
     const float zmax = __shfl_sync(0xffffffffu, zsel, 0);
     float ex = (lane < k) ? expf(zsel - zmax) : 0.0f;
