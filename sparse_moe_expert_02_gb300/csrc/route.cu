@@ -29,7 +29,9 @@ __device__ __forceinline__ float key_value(uint32_t k) {
     return __uint_as_float((k >> 31) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-template <int J>  // J = ceil(E / 32) logits per lane, a power of two
+// J = ceil(E / 32) logits per lane (a power of two); SB = K slices loaded per
+// batch (1 when the router GEMM did not split K: fewer registers, more warps)
+template <int J, int SB>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int S,
                                                    const float* __restrict__ bias, float* __restrict__ logits_out,
                                                    int T, int E, int k, int32_t* __restrict__ blob, uint32_t* err) {
@@ -41,7 +43,6 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
     // K-split partial products of the router GEMM (S slices): the loads of a
     // batch of SB slices are all issued before the first add, and the slices
     // are added in order
-    constexpr int SB = (J <= 16) ? 8 : 2;
     float v[J];
 #pragma unroll
     for (int j = 0; j < J; ++j) v[j] = 0.0f;
@@ -140,7 +141,12 @@ cudaError_t launch_topk(const float* part, int S, const float* bias, float* logi
     const int warps = 8;
     dim3 grid((unsigned)cdiv(T, warps)), block(32 * warps);
     const int J = (int)cdiv(E, 32);
-#define MOE_TOPK(JJ) topk_kernel<JJ><<<grid, block, 0, stream>>>(part, S, bias, logits_out, T, E, k, blob, err)
+#define MOE_TOPK(JJ)                                                                                        \
+    do {                                                                                                    \
+        if (S == 1) topk_kernel<JJ, 1><<<grid, block, 0, stream>>>(part, S, bias, logits_out, T, E, k, blob, err); \
+        else topk_kernel<JJ, (JJ <= 16 ? 8 : 2)><<<grid, block, 0, stream>>>(part, S, bias, logits_out, T, E, k, \
+                                                                            blob, err);                     \
+    } while (0)
     if (J <= 1) MOE_TOPK(1);
     else if (J <= 2) MOE_TOPK(2);
     else if (J <= 4) MOE_TOPK(4);
