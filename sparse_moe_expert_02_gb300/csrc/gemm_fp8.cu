@@ -6,12 +6,10 @@
 // higher-precision path.  Here: weights carry one fp32 scale per 128x128
 // block, activations one per token per 128 columns, so every 128-wide slice
 // of K has its own product of scales.  tcgen05.mma kind::f8f6f4 multiplies
-// one such slice into TMEM as two half-chunks (the two 128-column halves of
-// the 256 accumulator columns, 4 MMAs of N=128, K=32 each) in a ring of four
-// 128-column buffers; the epilogue warps read a half-chunk, multiply it by
-// s_a[row] * s_w[block] and add it to fp32 accumulators held in registers,
-// while the MMA runs up to two slices ahead (with two 256-column buffers the
-// mbarrier hand-offs between MMA and epilogue, not the work, set the pace).  The scales are not powers of two, so they cannot ride in the
+// one such slice (4 MMAs of K=32) into one of two TMEM chunk buffers; the
+// epilogue warps read the chunk, multiply it by s_a[row] * s_w[block] and add
+// it to fp32 accumulators held in registers, while the MMA fills the other
+// buffer.  The scales are not powers of two, so they cannot ride in the
 // MMA's own block-scale operands.
 //
 // Unit, ordering, ring and error handling follow gemm_tc.cu (128 rows x 256
@@ -28,7 +26,7 @@
 //     through shared memory, and h is written as E4M3 codes with one fp32
 //     scale per row and 128 features (the next GEMM's activation format).
 //   Plain (down): 256 output features = two 128-row weight blocks, one per
-//     half-chunk; each thread owns 64 columns of each; bf16 result.
+//     column half; the result is written as bf16.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -55,8 +53,7 @@ constexpr int kThreads = 128 + 32 * kEpiWarps;
 constexpr int kRegsLaunch = 168, kRegsLow = 40, kRegsHigh = 232;
 static_assert(4 * (kRegsLaunch - kRegsLow) == kEpiWarps * (kRegsHigh - kRegsLaunch), "register split must balance");
 static_assert(kThreads * kRegsLaunch <= 65536, "launch registers exceed the SM");
-constexpr int kBufCols = 128;             // TMEM columns per half-chunk buffer
-constexpr int kBufs = 4;                  // 4 x 128 = all 512 TMEM columns
+constexpr int kAccCols = 256;
 constexpr int kBoxRowsA = 16;
 constexpr uint32_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + 256 + 2 * 2 * 128 * 4;
 
@@ -107,12 +104,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sB = smem + kStages * kABytes;
     uint64_t* bars = (uint64_t*)(sB + kStages * kBBytes);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
-    const uint32_t cfull0 = smem_u32(bars + 2 * kStages), cempty0 = smem_u32(bars + 2 * kStages + kBufs);
-    const uint32_t drain = smem_u32(bars + 2 * kStages + 2 * kBufs);
+    const uint32_t cfull0 = smem_u32(bars + 2 * kStages), cempty0 = smem_u32(bars + 2 * kStages + 2);
+    const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
     // [2 unit parities][4 lane quarters]: amax exchange between the two warps
     // that hold the two column halves of the same 32 rows
-    const uint32_t xbar0 = smem_u32(bars + 2 * kStages + 2 * kBufs + 1);
-    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kStages + 2 * kBufs + 9);
+    const uint32_t xbar0 = smem_u32(bars + 2 * kStages + 5);
+    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kStages + 13);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
     float* s_amax = (float*)(smem + kStages * (kABytes + kBBytes) + 256);  // [2 units][2 halves][128 rows]
 
@@ -122,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(full0 + 8 * s, 1);
             mbar_init(empty0 + 8 * s, 1);
         }
-        for (int b = 0; b < kBufs; ++b) {
+        for (int b = 0; b < 2; ++b) {
             mbar_init(cfull0 + 8 * b, 1);
             mbar_init(cempty0 + 8 * b, kEpiWarps);
         }
@@ -133,7 +130,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (warp == 1) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(kBufs * kBufCols)
+                     "r"(2 * kAccCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -203,40 +200,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // ----------------------------------------------------- MMA issuer
             int stage = 0;
-            uint32_t phase = 0, hc = 0;  // hc: half-chunks issued
-            const uint32_t idesc = idesc_e4m3(BM, kBufCols);
+            uint32_t phase = 0, chunk = 0;
+            const uint32_t idesc = idesc_e4m3(BM, 256);
             bool ok = true;
             for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-                for (int kb = 0; kb < p.KB && ok; ++kb) {
-                    if (!mbar_wait(full0 + 8 * stage, phase, lim, abort_flag)) {
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    const uint32_t buf = chunk & 1u, cpar = (chunk >> 1) & 1u;
+                    if (!mbar_wait(full0 + 8 * stage, phase, lim, abort_flag) ||
+                        !mbar_wait(cempty0 + 8 * buf, cpar ^ 1u, lim, abort_flag)) {
                         record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 12, blockIdx.x, u);
                         *abort_flag = 1;
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    const uint32_t d = tmem_base + buf * kAccCols;
                     const uint64_t ad = umma_desc(smem_u32(sA + stage * kABytes));
                     const uint64_t bd = umma_desc(smem_u32(sB + stage * kBBytes));
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {  // B rows 128q..128q+127 -> one 128-column buffer
-                        const uint32_t buf = hc & (kBufs - 1), cpar = (hc / kBufs) & 1u;
-                        if (!mbar_wait(cempty0 + 8 * buf, cpar ^ 1u, lim, abort_flag)) {
-                            record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 15, blockIdx.x, u);
-                            *abort_flag = 1;
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t d = tmem_base + buf * kBufCols;
-                        const uint64_t bq = bd + (uint64_t)((q * 128 * BKB) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < BKB / 32; ++kk)  // K=32 E4M3 per MMA: 32 bytes along the row
-                            umma_e4m3(d, ad + (uint64_t)(kk * 2), bq + (uint64_t)(kk * 2), idesc, kk != 0);
-                        umma_commit(cfull0 + 8 * buf);
-                        ++hc;
-                    }
-                    if (!ok) break;
+                    for (int kk = 0; kk < BKB / 32; ++kk)  // K=32 E4M3 per MMA: 32 bytes along the row
+                        umma_e4m3(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, kk != 0);
                     umma_commit(empty0 + 8 * stage);
+                    umma_commit(cfull0 + 8 * buf);
+                    ++chunk;
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -255,7 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sub = warp & 3;      // TMEM lane quarter
         const int half = ew >> 2;      // which half of the columns
         const int row = sub * 32 + lane;
-        uint32_t hc = 0, nunit = 0;  // hc: half-chunks consumed
+        uint32_t chunk = 0, nunit = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++nunit) {
             const int unit_par = nunit & 1;
@@ -275,9 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (EPI == EPI_SWIGLU) {
                 wsc1 = p.b_scale + ((int64_t)un.g * nblocks + un.nb) * p.KB;
                 wsc2 = p.b2_scale + ((int64_t)un.g * nblocks + un.nb) * p.KB;
-            } else {  // the unit's 256 outputs are weight blocks 2nb and 2nb+1
-                wsc1 = p.b_scale + ((int64_t)un.g * nblocks + 2 * un.nb) * p.KB;
-                wsc2 = wsc1 + p.KB;
+            } else {
+                wsc1 = p.b_scale + ((int64_t)un.g * nblocks + 2 * un.nb + half) * p.KB;
+                wsc2 = wsc1;
             }
             float sa_next = __ldg(asc), s1_next = __ldg(wsc1), s2_next = __ldg(wsc2);
             for (int kb = 0; kb < p.KB; ++kb) {
@@ -287,32 +273,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                     s1_next = __ldg(wsc1 + kb + 1);
                     s2_next = __ldg(wsc2 + kb + 1);
                 }
+                const uint32_t buf = chunk & 1u, cpar = (chunk >> 1) & 1u;
+                int w_ok = 1;
+                if (lane == 0) {
+                    w_ok = mbar_wait(cfull0 + 8 * buf, cpar, lim, abort_flag);
+                    if (!w_ok) {
+                        record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 13, blockIdx.x, u);
+                        *abort_flag = 1;
+                    }
+                }
+                w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+                if (!w_ok) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t tb = tmem_base + ((uint32_t)(sub * 32) << 16) + buf * kAccCols;
                 const float f1 = sa * s1, f2 = sa * s2;
-                // Half-chunk q: SwiGLU q=0 gate / q=1 up, plain q = weight
-                // block 2nb+q.  This warp reads its 64 columns (64*half..) of
-                // each: two 32-column TMEM loads per wait, then the promotion
-                // with paired fp32 FMAs.
+                // Two 32-column TMEM loads per wait, then the promotion with
+                // paired fp32 FMAs (two lanes of work per instruction).
+                // SwiGLU: q=0 -> gate columns 64*half.., q=1 -> up columns
+                // 128+64*half..; plain: q -> columns 128*half + 64*q.
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    const uint32_t buf = hc & (kBufs - 1), cpar = (hc / kBufs) & 1u;
-                    int w_ok = 1;
-                    if (lane == 0) {
-                        w_ok = mbar_wait(cfull0 + 8 * buf, cpar, lim, abort_flag);
-                        if (!w_ok) {
-                            record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 13, blockIdx.x, u);
-                            *abort_flag = 1;
-                        }
-                    }
-                    w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-                    if (!w_ok) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
                     uint32_t r[64];
-                    tmem_ld32x2(tmem_base + ((uint32_t)(sub * 32) << 16) + buf * kBufCols + 64 * half, r);
+                    const int col = (EPI == EPI_SWIGLU) ? (q == 0 ? 64 * half : 128 + 64 * half) : 128 * half + 64 * q;
+                    tmem_ld32x2(tb + col, r);
                     tmem_wait_ld();
-                    const float f = q ? f2 : f1;
+                    const float f = (EPI == EPI_SWIGLU && q == 1) ? f2 : f1;
                     const float2 ff = make_float2(f, f);
 #pragma unroll
                     for (int i = 0; i < 64; i += 2) {
@@ -321,12 +309,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         acc[64 * q + i] = a.x;
                         acc[64 * q + i + 1] = a.y;
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(cempty0 + 8 * buf);
-                    ++hc;
                 }
-                if (!ok) break;
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cempty0 + 8 * buf);
+                ++chunk;
             }
             if (!ok) break;
             const int64_t orow = (int64_t)un.row0 + m;
@@ -373,15 +360,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (half == 0) p.out_scale[orow * nblocks + un.nb] = sc;
                 }
             } else if (valid) {
-                // acc[0..63]: outputs nb*256 + 64*half.., acc[64..127]: nb*256 + 128 + 64*half..
-                bf16* o = (bf16*)p.out + orow * p.ldo + un.nb * 256 + 64 * half;
+                bf16* o = (bf16*)p.out + orow * p.ldo + un.nb * 256 + 128 * half;
 #pragma unroll
                 for (int v = 0; v < 16; ++v) {
                     uint4 pk;
                     __nv_bfloat162* h2 = (__nv_bfloat162*)&pk;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) h2[j] = __floats2bfloat162_rn(acc[8 * v + 2 * j], acc[8 * v + 2 * j + 1]);
-                    *(uint4*)(o + (v < 8 ? 8 * v : 128 + 8 * (v - 8))) = pk;
+                    *(uint4*)(o + 8 * v) = pk;
                 }
             }
         }
@@ -392,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kBufs * kBufCols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * kAccCols)
                      : "memory");
     }
 }
