@@ -345,10 +345,17 @@ def run_reference(args, shape, world, rank, local):
     inp = synth.make_inputs(shape, seed=args.seed, device=dev)
     n = args.ref_tokens
     times = []
+    t_start = time.perf_counter()
     for i in range(args.warmup + args.steps):
         ntok, dt = oracle_sample(shape, inp, n, seed=100 + i)
         if i >= args.warmup:
             times.append(dt)
+        # keep the whole run to a few minutes: after the first step, shrink
+        # the per-step sample if the projected run would exceed ~3 min
+        if i == 0 and n > 1:
+            projected = (time.perf_counter() - t_start) * (args.warmup + args.steps)
+            if projected > 180.0:
+                n = max(1, int(n * 180.0 / projected))
     ms = sum(times) * 1e3
     value = ntok * args.steps / (ms / 1e3)
     cores = int(os.environ.get("OMP_NUM_THREADS", cpu_cores()))
@@ -382,7 +389,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample size for cpu_baseline")
     ap.add_argument("--experts", type=int, default=0,
                     help="override E (profiling captures on a few-GB copy of the workload); not a bench line")
-    ap.add_argument("--ref-tokens", type=int, default=4, help="oracle tokens per step for --impl reference")
+    ap.add_argument("--ref-tokens", type=int, default=2, help="oracle tokens per step for --impl reference")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

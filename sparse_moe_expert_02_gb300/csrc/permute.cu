@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(32) perm_rank_kernel(const int32_t* __restrict
 // 32nd of the pairs (histogram, then its ranks), thread e scans expert e over
 // the 32 warps.  Decode-sized routing (1280 pairs) spends ~5 us here instead
 // of four dependent launches.
-constexpr int kSmallPairs = 8192;
+constexpr int kSmallPairs = 16384;
 constexpr int kSmallMaxE = 512;
 constexpr int kSmallSmem = (32 * kSmallMaxE + 4 * (kSmallMaxE + 2)) * 4;
 

@@ -1,0 +1,75 @@
+"""Host-side pieces of bench.py, on the CPU: the multi-rank launch (gloo,
+world size 2) of the reference arm, the algorithmic byte/flop accounting and
+the clock-sample parser."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+from sparse_moe_expert_02_gb300 import synth  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_reference_arm_world_size_2_gloo():
+    """Under torchrun with two ranks, rank 0 alone times the oracle and prints
+    one JSON line; rank 1 exits 0 without output."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "3",
+           "--workload", synth.TINY_F32.name, "--ref-tokens", "2"]
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="2")
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["steps"] == 2 and d["warmup"] == 3
+    assert d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["dtype"] == "f64"
+
+
+def test_warmup_below_three_is_refused():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"], capture_output=True,
+                       text=True, timeout=120)
+    assert r.returncode != 0 and "warmup" in r.stderr
+
+
+def test_algorithmic_accounting():
+    shape = synth.DECODE_BF16
+    counts = np.zeros(shape.E + 1, np.int64)
+    counts[:475] = 1
+    a = bench.algorithmic(shape, counts)
+    D, I, E, T, k = shape.D, shape.I, shape.E, shape.T, shape.top_k
+    per_expert = 3 * D * I * 2
+    assert a["touched_experts"] == 475
+    assert a["layer_bytes"] == 476 * per_expert + E * D * 2 + T * D * 2 + T * D * 4 + 8 * T * k
+    assert a["flops"] == T * (2 * D * E + (k + 1) * 6 * D * I)
+    assert a["gemm_gateup_bytes"] > 476 * 2 * I * D * 2
+
+
+def test_clock_summary_keeps_samples_inside_the_timed_window(tmp_path):
+    c = bench.ClockSampler(0)
+    c.proc = object()
+    c.path = str(tmp_path / "clk.csv")
+    rows = [("2026/12/02 10:00:00.000", 1000), ("2026/12/02 10:00:01.000", 2000), ("2026/12/02 10:00:01.200", 2050),
+            ("2026/12/02 10:00:05.000", 900)]
+    with open(c.path, "w") as fh:
+        for ts, mhz in rows:
+            fh.write(f"{ts}, {mhz}, 2070, 900.0, 0x0, Not Active, Not Active, Not Active, Active\n")
+    import datetime
+    c.t_begin = datetime.datetime.strptime(rows[1][0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    c.t_end = datetime.datetime.strptime(rows[2][0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+    s = c.summary()
+    assert s["sm_mhz"] == 2025.0 and s["sm_max_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
