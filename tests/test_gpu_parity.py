@@ -148,6 +148,35 @@ def test_compact_routing_words_bit_exact():
     assert np.array_equal(words.cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("shape", [synth.SMALL_BF16, synth.SMALL_FP8], ids=["bf16", "fp8"])
+def test_forward_replays_from_a_cuda_graph(shape):
+    """moe_forward only enqueues work (no host sync), so a call captured in a
+    CUDA graph replays to the same output (after one eager call that does the
+    one-time kernel attribute set-up)."""
+    inp = _dev_inputs(shape, seed=12)
+    layer = MoELayer.from_shape(shape, inp, out_dtype="f32")
+    x = inp["x"].clone()
+    ref = layer.forward(x).clone()
+    out = layer.new_out(shape.T)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            layer.forward(x, out)
+    torch.cuda.current_stream().wait_stream(s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    x.copy_(torch.roll(inp["x"], 1, 0))   # new input through the same graph
+    g.replay()
+    ref2 = layer.forward(x)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref2)
+    layer.check()
+
+
 # ------------------------------------------------------------- stage tests
 
 @pytest.mark.parametrize("T,E,k", [(300, 16, 2), (1000, 512, 10), (37, 1000, 32), (5, 7, 7)])
