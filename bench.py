@@ -358,7 +358,8 @@ def run_reference(args, shape, world, rank, local):
                 n = max(1, int(n * 180.0 / projected))
     ms = sum(times) * 1e3
     value = ntok * args.steps / (ms / 1e3)
-    cores = int(os.environ.get("OMP_NUM_THREADS", cpu_cores()))
+    # the oracle parallelises over tokens: it keeps at most ntok threads busy
+    cores = min(ntok, int(os.environ.get("OMP_NUM_THREADS", cpu_cores())))
     sample = f"{ntok} of {shape.T} tokens per step, whole layer in fp64 (router, top-k, {shape.top_k} experts + shared)"
     return {
         "metric": "routed-MoE layer tokens/s at E=512,k=10,D=4096",
@@ -389,7 +390,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample size for cpu_baseline")
     ap.add_argument("--experts", type=int, default=0,
                     help="override E (profiling captures on a few-GB copy of the workload); not a bench line")
-    ap.add_argument("--ref-tokens", type=int, default=2, help="oracle tokens per step for --impl reference")
+    ap.add_argument("--ref-tokens", type=int, default=16, help="oracle tokens per step for --impl reference")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -415,7 +416,8 @@ def main():
             oracle.build()
             ntok, dt = oracle_sample(shape, inp, args.cpu_tokens)
             res["cpu_baseline"] = {"value": round(ntok / dt, 3), "unit": "tokens/s",
-                                   "cores": int(os.environ.get("OMP_NUM_THREADS", cpu_cores())), "kind": "oracle",
+                                   "cores": min(ntok, int(os.environ.get("OMP_NUM_THREADS", cpu_cores()))),
+                                   "kind": "oracle",
                                    "sample": f"{ntok} of {shape.T} tokens, whole layer in fp64 "
                                              f"(router, top-k, {shape.top_k} experts + shared), {dt:.1f} s"}
         if rank == 0:
