@@ -44,6 +44,9 @@
  *   w_down   [E+1, D, I]    same
  *   s_gate, s_up [E+1, I/128, D/128] and s_down [E+1, D/128, I/128]:
  *                           fp32 block scales, MOE_FP8_E4M3_B128 only.
+ *   w_down_f16 [E+1, D, I]  fp16 copy of w_down (MOE_BF16 layer on tensor
+ *                           cores, unless MOE_FLAG_DOWN_HILO); made once by
+ *                           moe_convert_down_weights().
  * Every matrix is [out_features, in_features]: the reduction dimension is
  * innermost (K-major), which is what the tensor-core operand loads want.
  */
@@ -72,15 +75,21 @@ typedef enum moe_status {
     MOE_ERR_CUDA = 4,           /* a CUDA runtime call or launch failed */
     MOE_ERR_DEVICE_TIMEOUT = 5, /* a bounded device wait ran out (moe_check) */
     MOE_ERR_BOUNDS = 6,         /* a device-side index check failed (moe_check) */
-    MOE_ERR_NONFINITE = 7       /* a router logit was NaN or infinite (moe_check) */
+    MOE_ERR_NONFINITE = 7       /* a router logit was NaN or infinite, or an fp16 h value
+                                   overflowed (diagnostic word 1 = 5) (moe_check) */
 } moe_status;
 
 /* Arithmetic type of the layer.
  *   MOE_F32: fp32 activations and weights, fp32 arithmetic throughout (no
  *     tensor cores).
- *   MOE_BF16: bf16 x and weights, fp32 accumulation; the permuted x is bf16,
- *     h is kept as a bf16 hi/lo pair and the expert outputs in fp32, so the
- *     layer stays within 1e-2 of the output rms; fp32 or bf16 output.
+ *   MOE_BF16: bf16 x and weights, fp32 accumulation; the permuted x is bf16
+ *     and the expert outputs fp32.  h = SiLU(gate)*up is rounded once to fp16
+ *     (11 significant bits) and the down GEMM reads an fp16 copy of W_down
+ *     (exact for every bf16 weight of magnitude 2^-14 .. 65504); |h| above
+ *     65504 is reported as MOE_ERR_NONFINITE.  With MOE_FLAG_DOWN_HILO h is
+ *     instead kept as a bf16 hi/lo pair against the bf16 W_down (no range
+ *     limit, twice the down-GEMM work).  Either way the layer stays within
+ *     1e-2 of the output rms; fp32 or bf16 output.
  *   MOE_FP8_E4M3_B128: expert weights as E4M3 codes with one fp32 scale per
  *     128x128 block; both expert GEMM inputs (x and h) quantised to E4M3 per
  *     token per 128-column group with s = amax/448 and
@@ -93,6 +102,7 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2 } moe_
 #define MOE_FLAG_FORCE_SIMT 0x1u   /* expert GEMMs on the CUDA-core kernel (cross-check path) */
 #define MOE_FLAG_PAIR_CTA_OFF 0x2u /* bf16 expert GEMMs never on CTA pairs (the default) */
 #define MOE_FLAG_PAIR_CTA_ON 0x4u  /* bf16 expert GEMMs on CTA pairs (cta_group::2, 256-row tiles) */
+#define MOE_FLAG_DOWN_HILO 0x8u    /* bf16 layer: h as a bf16 hi/lo pair, bf16 W_down (no w_down_f16) */
 
 typedef struct moe_config {
     int32_t T_max;           /* largest token count a call may pass */
@@ -113,6 +123,7 @@ typedef struct moe_weights {
     const float* s_gate;
     const float* s_up;
     const float* s_down;
+    const void* w_down_f16;  /* MOE_BF16 only (see above); NULL otherwise */
 } moe_weights;
 
 typedef struct moe_plan moe_plan;
@@ -237,6 +248,16 @@ MOE_API moe_status moe_permute_index_noalloc(const int32_t* idx, int32_t T, int3
  * two-plane blob; the weight keeps 8 significant bits. */
 MOE_API moe_status moe_pack_routing_words(const moe_plan* plan, int32_t T, const void* ws, size_t ws_bytes,
                                           int32_t* words, void* stream);
+
+/* One-time weight preparation of the bf16 layer: writes w_down_f16, the
+ * fp16 copy of w_down ([E+1, D, I], both caller-allocated device buffers,
+ * 16-byte aligned, not overlapping) that the down GEMM reads on tensor cores.
+ * Each value is rounded to nearest even; bf16 values below 2^-14 in
+ * magnitude lose low bits (fp16 subnormals), values above 65504 record
+ * MOE_ERR_BOUNDS in the error word of `ws` (moe_check reports it).
+ * MOE_ERR_UNSUPPORTED unless the plan's dtype is MOE_BF16. */
+MOE_API moe_status moe_convert_down_weights(const moe_plan* plan, const void* w_down, void* w_down_f16, void* ws,
+                                            size_t ws_bytes, void* stream);
 
 /* Synchronise `stream`, read the workspace error word and return the first
  * device-side error recorded since the last clear (MOE_OK if none). */

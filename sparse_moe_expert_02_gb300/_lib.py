@@ -27,6 +27,7 @@ MOE_F32, MOE_BF16, MOE_FP8_E4M3_B128 = 0, 1, 2
 MOE_FLAG_FORCE_SIMT = 0x1
 MOE_FLAG_PAIR_CTA_OFF = 0x2
 MOE_FLAG_PAIR_CTA_ON = 0x4
+MOE_FLAG_DOWN_HILO = 0x8
 
 DTYPE_CODE = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8": MOE_FP8_E4M3_B128}
 
@@ -36,7 +37,7 @@ SYMBOLS = (
     "moe_workspace_init", "moe_quantize_weights", "moe_forward", "moe_route", "moe_topk", "moe_permute",
     "moe_gemm_gateup", "moe_gemm_down", "moe_unpermute", "moe_check", "moe_selftest_wait_timeout",
     "moe_status_str", "moe_last_error_detail", "moe_build_info", "moe_launch_count",
-    "moe_permute_index_noalloc", "moe_pack_routing_words",
+    "moe_permute_index_noalloc", "moe_pack_routing_words", "moe_convert_down_weights",
 )
 
 
@@ -48,7 +49,7 @@ class moe_config(ctypes.Structure):
 
 class moe_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
-                ("w_router", "b_router", "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down")]
+                ("w_router", "b_router", "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down", "w_down_f16")]
 
 
 class moe_ws_layout(ctypes.Structure):
@@ -102,6 +103,7 @@ def lib():
                 "moe_launch_count": (ctypes.c_uint64, []),
                 "moe_permute_index_noalloc": (st, [P, I32, I32, I32, P, P, P, P, P, P]),
                 "moe_pack_routing_words": (st, [P, I32, P, S, P, P]),
+                "moe_convert_down_weights": (st, [P, P, P, P, S, P]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -172,9 +174,14 @@ def moe_quantize_weights(plan, w, q, s, stream=None):
         "moe_quantize_weights")
 
 
+def moe_convert_down_weights(plan, w_down, w_down_f16, ws, stream=None):
+    _ok(lib().moe_convert_down_weights(plan, _ptr(w_down), _ptr(w_down_f16), _ptr(ws), _wsb(ws), _stream(stream)),
+        "moe_convert_down_weights")
+
+
 def make_weights(w: dict) -> moe_weights:
     return moe_weights(*[_ptr(w.get(n)) for n in
-                         ("w_router", "b_router", "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down")])
+                         ("w_router", "b_router", "w_gate", "w_up", "w_down", "s_gate", "s_up", "s_down", "w_down_f16")])
 
 
 def _wsb(ws):

@@ -27,7 +27,7 @@ namespace {
 thread_local char g_detail[256];
 
 moe_status cuda_fail(cudaError_t e, const char* where) {
-    snprintf(g_detail, sizeof(g_detail), "%s: %s", where, cudaGetErrorString(e));
+    snprintf(g_detail, sizeof(g_detail), "%.160s: %s", where, cudaGetErrorString(e));
     return MOE_ERR_CUDA;
 }
 moe_status arg_fail(moe_status s, const char* what) {
@@ -42,6 +42,11 @@ moe_status arg_fail(moe_status s, const char* what) {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// bf16 layer: h as a bf16 hi/lo pair against the bf16 W_down (on request),
+// else h as one fp16 against an fp16 copy of W_down.
+bool hilo(const moe_config& c) { return c.dtype == MOE_BF16 && (c.flags & MOE_FLAG_DOWN_HILO); }
+bool f16_down(const moe_config& c) { return c.dtype == MOE_BF16 && !(c.flags & MOE_FLAG_DOWN_HILO); }
 
 int act_bytes(int dtype) { return dtype == MOE_F32 ? 4 : (dtype == MOE_BF16 ? 2 : 1); }
 int act_elem(int dtype) { return dtype == MOE_F32 ? moe::kF32 : (dtype == MOE_BF16 ? moe::kBF16 : moe::kE4M3); }
@@ -75,7 +80,7 @@ void layout(const moe_config& c, int num_sms, int T, moe_ws_layout* L) {
     // bf16 layer: h is a bf16 hi/lo pair per element ([R, 2I]); the pair
     // keeps the down GEMM's input at ~fp32 precision (a single bf16 rounding
     // of h alone costs about 1e-2 of the output rms).
-    L->h = take((size_t)R * c.I * (c.dtype == MOE_BF16 ? 4 : ab));
+    L->h = take((size_t)R * c.I * (hilo(c) ? 4 : ab));
     L->h_scale = fp8 ? take((size_t)R * (c.I / 128) * 4) : 0;
     // y in fp32 except for the FP8 layer (bf16 there): a bf16 y alone costs
     // about 1.3e-2 of the output rms, above the bf16 layer's tolerance.
@@ -117,6 +122,8 @@ moe_status check_weights(const moe_plan* p, const moe_weights* w, bool router, b
     if (experts) {
         if (!ptr_ok(w->w_gate) || !ptr_ok(w->w_up) || !ptr_ok(w->w_down))
             return arg_fail(MOE_ERR_INVALID_ARG, "expert weight NULL or misaligned");
+        if (f16_down(p->cfg) && !(p->cfg.flags & MOE_FLAG_FORCE_SIMT) && !ptr_ok(w->w_down_f16))
+            return arg_fail(MOE_ERR_INVALID_ARG, "w_down_f16 NULL or misaligned (see moe_convert_down_weights)");
         if (p->cfg.dtype == MOE_FP8_E4M3_B128 && (!ptr_ok(w->s_gate) || !ptr_ok(w->s_up) || !ptr_ok(w->s_down)))
             return arg_fail(MOE_ERR_INVALID_ARG, "FP8 block scales NULL or misaligned");
     }
@@ -357,7 +364,7 @@ moe_status moe_gemm_gateup(const moe_plan* p, const moe_weights* w, const void* 
     g.prefer_pairs = prefer_pairs(p, T);
     g.N = c.I;
     g.Ka = g.Kb = c.D;
-    g.out_pair = c.dtype == MOE_BF16;
+    g.out_pair = hilo(c);
     g.ldo = g.out_pair ? 2 * c.I : c.I;
     g.a_rows = T * c.top_k;
     g.a_shared_rows = T;
@@ -371,7 +378,7 @@ moe_status moe_gemm_gateup(const moe_plan* p, const moe_weights* w, const void* 
     g.b_scale = w->s_gate;
     g.b2_scale = w->s_up;
     g.out = W.at<void>(W.L.h);
-    g.out_elem = act_elem(c.dtype);
+    g.out_elem = f16_down(c) ? moe::kF16 : act_elem(c.dtype);
     g.out_scale = fp8 ? W.at<float>(W.L.h_scale) : nullptr;
     g.err = W.at<uint32_t>(W.L.err);
     g.spin_ns = p->spin_ns;
@@ -397,13 +404,18 @@ moe_status moe_gemm_down(const moe_plan* p, const moe_weights* w, int32_t T, voi
     g.prefer_pairs = prefer_pairs(p, T);
     g.N = c.D;
     g.Kb = c.I;
-    g.Ka = (c.dtype == MOE_BF16) ? 2 * c.I : c.I;  // hi/lo pair walks W_down twice
+    g.Ka = hilo(c) ? 2 * c.I : c.I;  // the hi/lo pair walks W_down twice
     g.ldo = c.D;
     g.a_rows = T * (c.top_k + 1);
     g.elem = act_elem(c.dtype);
     g.a = W.at<void>(W.L.h);
     g.a_scale = fp8 ? W.at<float>(W.L.h_scale) : nullptr;
     g.b = w->w_down;
+    if (f16_down(c)) {
+        g.elem = moe::kF16;  // fp16 h
+        if (c.flags & MOE_FLAG_FORCE_SIMT) g.b_elem = moe::kBF16;  // CUDA cores read the bf16 W_down
+        else g.b = w->w_down_f16;                                   // tensor cores: one type for A and B
+    }
     g.b_scale = w->s_down;
     g.out = W.at<void>(W.L.y);
     g.out_elem = fp8 ? moe::kBF16 : moe::kF32;
@@ -447,6 +459,17 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
                                  cudaMemcpyDeviceToDevice, s));
     if (logits_out)
         MOE_CUDA(cudaMemcpyAsync(logits_out, W.at<float>(W.L.logits), (size_t)T * c.E * 4, cudaMemcpyDeviceToDevice, s));
+    return MOE_OK;
+}
+
+moe_status moe_convert_down_weights(const moe_plan* p, const void* w_down, void* w_down_f16, void* ws,
+                                   size_t ws_bytes, void* stream) {
+    if (!p) return arg_fail(MOE_ERR_INVALID_ARG, "plan is NULL");
+    if (p->cfg.dtype != MOE_BF16) return arg_fail(MOE_ERR_UNSUPPORTED, "only the bf16 layer has an fp16 W_down copy");
+    if (!ptr_ok(w_down) || !ptr_ok(w_down_f16)) return arg_fail(MOE_ERR_INVALID_ARG, "NULL or misaligned pointer");
+    if (!ws || !aligned(ws, 256) || ws_bytes < 256) return arg_fail(MOE_ERR_INVALID_ARG, "workspace");
+    const int64_t n = (int64_t)(p->cfg.E + 1) * p->cfg.D * p->cfg.I;
+    MOE_CUDA(moe::launch_bf16_to_f16(w_down, w_down_f16, n, (uint32_t*)ws, (cudaStream_t)stream));
     return MOE_OK;
 }
 

@@ -12,6 +12,7 @@
 namespace moe {
 
 typedef __nv_bfloat16 bf16;
+typedef __half f16;
 
 // ---------------------------------------------------------------- errors
 
@@ -38,10 +39,12 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(bf16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float to_f32(f16 v) { return __half2float(v); }
 
 template <typename T> __device__ __forceinline__ T from_f32(float v);
 template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <> __device__ __forceinline__ bf16 from_f32<bf16>(float v) { return __float2bfloat16_rn(v); }
+template <> __device__ __forceinline__ f16 from_f32<f16>(float v) { return __float2half_rn(v); }
 
 // E4M3, round to nearest even, saturating to +-448.
 __device__ __forceinline__ uint8_t f32_to_e4m3(float v) {

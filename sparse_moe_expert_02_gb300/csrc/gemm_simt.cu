@@ -7,6 +7,7 @@
 // gate and up products share the A tile).  Row tiles of the grouped layout
 // are walked through the device-built tile prefix, so no host round trip
 // is needed to learn the per-expert row counts.
+#include <type_traits>
 #include <algorithm>
 
 #include "common.cuh"
@@ -28,13 +29,19 @@ template <> __device__ __forceinline__ void load8<bf16>(const bf16* p, float* v)
 #pragma unroll
     for (int i = 0; i < 8; ++i) v[i] = __bfloat162float(e[i]);
 }
+template <> __device__ __forceinline__ void load8<f16>(const f16* p, float* v) {
+    int4 r = __ldg((const int4*)p);
+    const f16* e = (const f16*)&r;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __half2float(e[i]);
+}
 template <typename T> __device__ __forceinline__ void load4(const T* p, float* v) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = to_f32(p[i]);
 }
 }  // namespace
 
-template <typename TE, typename TO, bool SWIGLU>
+template <typename TE, typename TB, typename TO, bool SWIGLU>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GroupedGemm g) {
     __shared__ float As[BK][BM + 4];
     __shared__ float Bs[BK][BN + 4];
@@ -58,8 +65,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GroupedGemm g) {
             nrows = g.rows;
         }
         const TE* abase = (grp == g.shared_group) ? As_ : A + (int64_t)out0 * Ka;
-        const TE* b1 = (const TE*)g.b + (int64_t)grp * N * Kb;
-        const TE* b2 = SWIGLU ? (const TE*)g.b2 + (int64_t)grp * N * Kb : nullptr;
+        const TB* b1 = (const TB*)g.b + (int64_t)grp * N * Kb;
+        const TB* b2 = SWIGLU ? (const TB*)g.b2 + (int64_t)grp * N * Kb : nullptr;
         float acc[8][4], acc2[SWIGLU ? 8 : 1][4];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
@@ -79,8 +86,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GroupedGemm g) {
                 for (int i = 0; i < 8; ++i) av[i] = 0.f;
             }
             if (b_ok) {
-                load4<TE>(b1 + (int64_t)(n0 + br) * Kb + kb0 + bk, bv);
-                if (SWIGLU) load4<TE>(b2 + (int64_t)(n0 + br) * Kb + kb0 + bk, bv2);
+                load4<TB>(b1 + (int64_t)(n0 + br) * Kb + kb0 + bk, bv);
+                if (SWIGLU) load4<TB>(b2 + (int64_t)(n0 + br) * Kb + kb0 + bk, bv2);
             } else {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) { bv[i] = 0.f; bv2[i] = 0.f; }
@@ -125,6 +132,8 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GroupedGemm g) {
                 float v = SWIGLU ? swiglu(acc[i][j], acc2[i][j]) : acc[i][j];
                 if (g.bias) v += __ldg(g.bias + n);
                 const int64_t o = (int64_t)(out0 + m) * g.ldo + n;
+                if (std::is_same<TO, f16>::value && !(fabsf(v) <= 65504.f))
+                    record_error(g.err, MOE_ERR_NONFINITE, 5, blockIdx.x, 1);
                 const TO hi = from_f32<TO>(v);
                 out[o] = hi;
                 if (g.out_pair) out[o + N] = from_f32<TO>(v - to_f32(hi));
@@ -138,21 +147,19 @@ cudaError_t launch_gemm_simt(const GroupedGemm& g, cudaStream_t stream) {
     if (g.max_tiles <= 0) return cudaGetLastError();
     dim3 grid((unsigned)std::min(g.max_tiles, 4096), (unsigned)cdiv(g.N, BN)), block(256);
     const bool sw = g.b2 != nullptr;
-    if (g.elem == kF32) {
-        if (g.out_elem != kF32) return cudaErrorInvalidValue;
-        if (sw) gemm_simt_kernel<float, float, true><<<grid, block, 0, stream>>>(g);
-        else gemm_simt_kernel<float, float, false><<<grid, block, 0, stream>>>(g);
-    } else if (g.elem == kBF16) {
-        if (g.out_elem == kF32) {
-            if (sw) gemm_simt_kernel<bf16, float, true><<<grid, block, 0, stream>>>(g);
-            else gemm_simt_kernel<bf16, float, false><<<grid, block, 0, stream>>>(g);
-        } else {
-            if (sw) gemm_simt_kernel<bf16, bf16, true><<<grid, block, 0, stream>>>(g);
-            else gemm_simt_kernel<bf16, bf16, false><<<grid, block, 0, stream>>>(g);
-        }
-    } else {
-        return cudaErrorInvalidValue;
-    }
+    const int be = g.b_elem > 0 ? g.b_elem : g.elem;
+#define MOE_SIMT(TA, TBB, TO)                                                          \
+    do {                                                                              \
+        if (sw) gemm_simt_kernel<TA, TBB, TO, true><<<grid, block, 0, stream>>>(g);   \
+        else gemm_simt_kernel<TA, TBB, TO, false><<<grid, block, 0, stream>>>(g);     \
+    } while (0)
+    if (g.elem == kF32 && be == kF32 && g.out_elem == kF32) MOE_SIMT(float, float, float);
+    else if (g.elem == kBF16 && be == kBF16 && g.out_elem == kF32) MOE_SIMT(bf16, bf16, float);
+    else if (g.elem == kBF16 && be == kBF16 && g.out_elem == kBF16) MOE_SIMT(bf16, bf16, bf16);
+    else if (g.elem == kBF16 && be == kBF16 && g.out_elem == kF16) MOE_SIMT(bf16, bf16, f16);
+    else if (g.elem == kF16 && be == kBF16 && g.out_elem == kF32) MOE_SIMT(f16, bf16, float);
+    else return cudaErrorInvalidValue;
+#undef MOE_SIMT
     count_launches(1);
     return cudaGetLastError();
 }

@@ -76,6 +76,8 @@ struct Params {
     int ldo;
     int out_pair;
     int out_f32;
+    int out_f16;         // SwiGLU output as fp16 (single rounding) instead of bf16
+    int in_f16;          // A and B are fp16 (else bf16)
     void* out;
     const float* bias;
     uint32_t* err;
@@ -108,6 +110,17 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u, int total_ti
         r.nrows = p.rows;
     }
     return r;
+}
+
+__device__ __forceinline__ void store_f16x32(f16* dst, const float* v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 pk;
+        __half2* h2 = (__half2*)&pk;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h2[i] = __floats2half2_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+        *(uint4*)(dst + 8 * q) = pk;
+    }
 }
 
 __device__ __forceinline__ void store_bf16x32(bf16* dst, const float* v) {
@@ -235,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ------------------------------------------------- MMA issuer
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
-            const uint32_t idesc = idesc_bf16(BM, p.BN);
+            const uint32_t idesc = p.in_f16 ? idesc_f16(BM, p.BN) : idesc_bf16(BM, p.BN);
             bool ok = true;
             for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
                 if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, lim, abort_flag)) {
@@ -318,6 +331,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float h[32], lo[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) h[i] = swiglu(__uint_as_float(gr[i]), __uint_as_float(ur[i]));
+                        if (p.out_f16) {
+                            float m = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(h[i]));
+                            if (!(m <= 65504.f)) record_error(p.err, MOE_ERR_NONFINITE, 5, blockIdx.x, 0);
+                            store_f16x32((f16*)o + c, h);
+                            continue;
+                        }
                         store_bf16x32(o + c, h);
                         if (p.out_pair) {
 #pragma unroll
@@ -393,7 +414,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 2D bf16 tensor [rows, cols] row-major, box {64 cols, box_rows}, 128B swizzle.
+// 2D tensor of 2-byte elements [rows, cols] row-major, box {64 cols,
+// box_rows}, 128B swizzle.  TMA copies bytes without conversion, so the map
+// serves bf16 and fp16 data alike.
 bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
     auto fn = encode_fn();
     if (!fn || rows < 1) return false;
@@ -434,13 +457,15 @@ cudaError_t launch_one(int grid, const CUtensorMap& ma, const CUtensorMap& msh, 
 
 bool gemm_tc_supported(const GroupedGemm& g) {
     using namespace tc;
-    if (g.elem != kBF16) return false;
+    if (g.elem != kBF16 && g.elem != kF16) return false;
+    if (g.b_elem > 0 && g.b_elem != g.elem) return false;  // the tensor cores take one type for A and B
     if (!encode_fn()) return false;
     if (g.Kb % BK || g.Kb < BK || (g.Ka != g.Kb && g.Ka != 2 * g.Kb)) return false;
     if (g.b2 && g.Ka != g.Kb) return false;  // the hi/lo pair is only the down GEMM's input
     if (!aligned16(g.a) || !aligned16(g.b) || !aligned16(g.out)) return false;
     if (g.b2) {  // SwiGLU
-        if (g.N % 128 || g.out_elem != kBF16 || g.bias) return false;
+        if (g.N % 128 || (g.out_elem != kBF16 && g.out_elem != kF16) || g.bias) return false;
+        if (g.out_elem == kF16 && g.out_pair) return false;
         if (!aligned16(g.b2) || (g.a_shared && !aligned16(g.a_shared))) return false;
     } else {
         if (!plain_bn(g.N) || g.out_pair) return false;
@@ -481,6 +506,8 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     p.ldo = g.ldo;
     p.out_pair = g.out_pair;
     p.out_f32 = g.out_elem == kF32;
+    p.out_f16 = g.out_elem == kF16;
+    p.in_f16 = g.elem == kF16;
     p.out = g.out;
     p.bias = g.bias;
     p.err = g.err;

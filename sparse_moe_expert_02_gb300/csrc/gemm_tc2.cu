@@ -53,7 +53,7 @@ struct Params {
     int G, shared_group;
     const int32_t* offsets;
     const int32_t* tiles2;  // prefix of ceil(rows/256)
-    int NB, N, KB, a_lo_x, ldo, out_pair, out_f32;
+    int NB, N, KB, a_lo_x, ldo, out_pair, out_f32, out_f16, in_f16;
     void* out;
     uint32_t* err;
     int64_t spin_ns;
@@ -77,6 +77,17 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
 __device__ __forceinline__ int boxes_for(int nrows, int m0) {
     const int valid = max(0, min(BM, nrows - m0));
     return (valid + kBoxRowsA - 1) / kBoxRowsA;
+}
+
+__device__ __forceinline__ void store_f16x32(f16* dst, const float* v) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 pk;
+        __half2* h2 = (__half2*)&pk;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h2[i] = __floats2half2_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+        *(uint4*)(dst + 8 * q) = pk;
+    }
 }
 
 __device__ __forceinline__ void store_bf16x32(bf16* dst, const float* v) {
@@ -194,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ------------------------------------------ MMA issuer (leader only)
             int stage = 0, acc = 0;
             uint32_t phase = 0, acc_phase = 0;
-            const uint32_t idesc = idesc_bf16(2 * BM, 256);
+            const uint32_t idesc = p.in_f16 ? idesc_f16(2 * BM, 256) : idesc_bf16(2 * BM, 256);
             for (int u = cid; u < total_units && !aborted; u += nclusters) {
                 if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, lim, abort_flag)) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 22, blockIdx.x, u);
@@ -275,6 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float h[32], lo[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) h[i] = swiglu(__uint_as_float(gr[i]), __uint_as_float(ur[i]));
+                        if (p.out_f16) {
+                            float m = 0.f;
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(h[i]));
+                            if (!(m <= 65504.f)) record_error(p.err, MOE_ERR_NONFINITE, 5, blockIdx.x, 0);
+                            store_f16x32((f16*)o + c, h);
+                            continue;
+                        }
                         store_bf16x32(o + c, h);
                         if (p.out_pair) {
 #pragma unroll
@@ -392,6 +411,8 @@ cudaError_t launch_gemm_tc2(const GroupedGemm& g, int num_sms, cudaStream_t stre
     p.ldo = g.ldo;
     p.out_pair = g.out_pair;
     p.out_f32 = g.out_elem == kF32;
+    p.out_f16 = g.out_elem == kF16;
+    p.in_f16 = g.elem == kF16;
     p.out = g.out;
     p.err = g.err;
     p.spin_ns = g.spin_ns > 0 ? g.spin_ns : 2000000000LL;

@@ -17,7 +17,7 @@ constexpr int kPermChunk = 1024;   // (t, j) pairs per permute chunk (largest si
 __host__ __device__ constexpr int perm_chunk(int64_t TK) { return TK <= 16384 ? 128 : kPermChunk; }
 
 // Element kinds of the GEMM operands.
-enum Elem : int { kF32 = 0, kBF16 = 1, kE4M3 = 2 };
+enum Elem : int { kF32 = 0, kBF16 = 1, kE4M3 = 2, kF16 = 3 };
 
 // One grouped GEMM, C_g = A_g * B_g^T, over the groups of the expert-grouped
 // row layout (or a single dense group).
@@ -41,7 +41,8 @@ struct GroupedGemm {
     int ldo;                     // output row stride in elements
     int out_pair;                // 1: bf16 output split as hi | lo halves (hi at col n, lo at col N+n)
     int a_rows, a_shared_rows;   // rows of the A tensors (tensor-map extents)
-    int elem;                    // Elem of A and B
+    int elem;                    // Elem of A (and of B when b_elem < 0)
+    int b_elem;                  // Elem of B when it differs from A (SIMT only); 0 = same as A
     const void* a;               // [*, K]
     const void* a_shared;        // [*, K]
     const float* a_scale;        // FP8: [*, K/128] per-row group scales of a
@@ -92,6 +93,9 @@ cudaError_t launch_quant_rows(const void* x, int x_elem, int rows, int cols, uin
                               cudaStream_t stream);
 cudaError_t launch_quant_blocks(const float* w, int64_t groups, int rows, int cols, uint8_t* q, float* s,
                                 cudaStream_t stream);
+// bf16 -> fp16 (round to nearest even); values outside fp16's finite range
+// record MOE_ERR_BOUNDS (their fp16 would not stand for the same weight).
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, int64_t n, uint32_t* err, cudaStream_t stream);
 cudaError_t launch_unpermute(const void* y, int y_elem, const int32_t* blob, const int32_t* inv, int T, int D,
                              int k, void* out, int out_elem, uint32_t* err, cudaStream_t stream);
 cudaError_t launch_selftest_timeout(uint32_t* err, int64_t limit_ns, cudaStream_t stream);

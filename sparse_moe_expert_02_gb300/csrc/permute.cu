@@ -348,6 +348,26 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(const float* __restri
     }
 }
 
+// bf16 -> fp16 for the down projection's tensor-core copy.  Every bf16 of
+// magnitude 2^-17 .. 65504 is an fp16 exactly (fp16 keeps 3 more mantissa
+// bits); smaller magnitudes round to fp16's subnormal grid (2^-24).  A finite
+// bf16 beyond 65504 has no fp16: it is recorded as MOE_ERR_BOUNDS.
+__global__ void bf16_to_f16_kernel(const bf16* __restrict__ src, f16* __restrict__ dst, int64_t n, uint32_t* err) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float v = __bfloat162float(src[i]);
+        if (isfinite(v) && fabsf(v) > 65504.0f) record_error(err, MOE_ERR_BOUNDS, (uint32_t)(i & 0xffffffff), 0, 3);
+        dst[i] = __float2half_rn(v);
+    }
+}
+
+cudaError_t launch_bf16_to_f16(const void* src, void* dst, int64_t n, uint32_t* err, cudaStream_t stream) {
+    if (n <= 0) return cudaGetLastError();
+    const int blocks = (int)std::min<int64_t>(cdiv(n, 256), 152 * 64);
+    bf16_to_f16_kernel<<<blocks, 256, 0, stream>>>((const bf16*)src, (f16*)dst, n, err);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_quant_blocks(const float* w, int64_t groups, int rows, int cols, uint8_t* q, float* s,
                                 cudaStream_t stream) {
     int64_t nb = groups * (rows / 128) * (cols / 128);

@@ -41,10 +41,20 @@ class MoELayer:
         else:
             for n in ("w_gate", "w_up", "w_down"):
                 w[n] = weights[n]
-        self.w = w
-        self.cw = L.make_weights(w)
         self.ws = torch.empty(L.moe_workspace_size(self.plan, T_max), dtype=torch.uint8, device=dev)
         L.moe_workspace_init(self.plan, self.ws)
+        self.hilo = dtype == "bf16" and bool(flags & L.MOE_FLAG_DOWN_HILO)
+        if dtype == "bf16" and not self.hilo and w.get("w_down") is not None:
+            if weights.get("w_down_f16") is not None:
+                w["w_down_f16"] = weights["w_down_f16"]
+            else:
+                wd = w["w_down"].contiguous()
+                w["w_down"] = wd
+                w["w_down_f16"] = torch.empty(wd.shape, dtype=torch.float16, device=dev)
+                L.moe_convert_down_weights(self.plan, wd, w["w_down_f16"], self.ws)
+                L.moe_check(self.plan, self.ws)
+        self.w = w
+        self.cw = L.make_weights(w)
 
     @classmethod
     def from_shape(cls, shape, inputs: dict, T_max: int = None, **kw):
@@ -113,7 +123,8 @@ class MoELayer:
         TK, R = T * k, T * k + T
         act = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.uint8}[self.dtype]
         ydt = torch.bfloat16 if self.dtype == "fp8" else torch.float32
-        hcols = 2 * I if self.dtype == "bf16" else I
+        hcols = 2 * I if self.hilo else I
+        hdt = torch.float16 if self.dtype == "bf16" and not self.hilo else act
         v = {
             "err": self.ws_view(T, "err", torch.int32, (4,)),
             "logits": self.ws_view(T, "logits", torch.float32, (T, E)),
@@ -124,7 +135,7 @@ class MoELayer:
             "inv": self.ws_view(T, "inv", torch.int32, (TK,)),
             "src_tok": self.ws_view(T, "src_tok", torch.int32, (R,)),
             "xp": self.ws_view(T, "xp", act, (TK, D)),
-            "h": self.ws_view(T, "h", act, (R, hcols)),
+            "h": self.ws_view(T, "h", hdt, (R, hcols)),
             "y": self.ws_view(T, "y", ydt, (R, D)),
         }
         if self.dtype == "fp8":

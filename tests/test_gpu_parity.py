@@ -99,8 +99,9 @@ def test_small_fp32_ragged(T):
     _layer_parity(shape, _dev_inputs(shape, seed=3))
 
 
-@pytest.mark.parametrize("flags", [0, L.MOE_FLAG_FORCE_SIMT, L.MOE_FLAG_PAIR_CTA_ON],
-                         ids=["default", "simt", "cta_pairs"])
+@pytest.mark.parametrize("flags", [0, L.MOE_FLAG_FORCE_SIMT, L.MOE_FLAG_PAIR_CTA_ON, L.MOE_FLAG_DOWN_HILO,
+                                   L.MOE_FLAG_DOWN_HILO | L.MOE_FLAG_FORCE_SIMT],
+                         ids=["default", "simt", "cta_pairs", "hilo", "hilo_simt"])
 @pytest.mark.parametrize("T", [300, 1, 128, 129, 700])
 def test_small_bf16_layer(flags, T):
     shape = synth.SMALL_BF16.with_tokens(T)
@@ -276,6 +277,31 @@ def test_nonfinite_logit_is_reported():
     layer = MoELayer.from_shape(shape, inp)
     layer.forward(inp["x"])
     assert L.moe_check_status(layer.plan, layer.ws) == L.MOE_ERR_NONFINITE
+
+
+def test_bf16_fp16_h_overflow_is_reported():
+    """fp16 h holds |h| <= 65504: beyond that the layer reports, and the
+    hi/lo pair path (no range limit) still matches the oracle."""
+    shape = synth.SMALL_BF16.with_tokens(64)
+    inp = _dev_inputs(shape, seed=7)
+    inp["x"] = (inp["x"].float() * 400.0).to(torch.bfloat16)
+    layer = MoELayer.from_shape(shape, inp)
+    layer.forward(inp["x"])
+    assert L.moe_check_status(layer.plan, layer.ws) == L.MOE_ERR_NONFINITE
+    assert int(layer.views(64)["err"][1]) == 5
+    _, out, _ = _layer_parity(shape, inp, flags=L.MOE_FLAG_DOWN_HILO, check_y=False)
+    assert torch.isfinite(out).all()
+
+
+def test_convert_down_weights_exact():
+    """bf16 -> fp16 copy of W_down: exact for every normal-range value."""
+    shape = synth.SMALL_BF16
+    inp = _dev_inputs(shape, seed=9)
+    layer = MoELayer.from_shape(shape, inp)
+    wd, wf = layer.w["w_down"], layer.w["w_down_f16"]
+    ref = wd.float()
+    assert torch.equal(wf.float()[ref.abs() >= 2.0 ** -14], ref[ref.abs() >= 2.0 ** -14])
+    assert (wf.float() - ref).abs().max().item() <= 2.0 ** -25
 
 
 def test_host_argument_errors():
