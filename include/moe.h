@@ -76,18 +76,19 @@ typedef enum moe_status {
     MOE_ERR_DEVICE_TIMEOUT = 5, /* a bounded device wait ran out (moe_check) */
     MOE_ERR_BOUNDS = 6,         /* a device-side index check failed (moe_check) */
     MOE_ERR_NONFINITE = 7       /* a router logit was NaN or infinite, or an fp16 h value
-                                   overflowed (diagnostic word 1 = 5) (moe_check) */
+                                   overflowed (diagnostic word 1 = 5 / 6) (moe_check) */
 } moe_status;
 
 /* Arithmetic type of the layer.
  *   MOE_F32: fp32 activations and weights, fp32 arithmetic throughout (no
  *     tensor cores).
- *   MOE_BF16: bf16 x and weights, fp32 accumulation; the permuted x is bf16
- *     and the expert outputs fp32.  h = SiLU(gate)*up is rounded once to fp16
- *     (11 significant bits) and the down GEMM reads an fp16 copy of W_down
- *     (exact for every bf16 weight of magnitude 2^-14 .. 65504); |h| above
- *     65504 is reported as MOE_ERR_NONFINITE.  With MOE_FLAG_DOWN_HILO h is
- *     instead kept as a bf16 hi/lo pair against the bf16 W_down (no range
+ *   MOE_BF16: bf16 x and weights, fp32 accumulation; the permuted x is bf16.
+ *     h = SiLU(gate)*up and the expert outputs y are each rounded once to
+ *     fp16 (11 significant bits), and the down GEMM reads an fp16 copy of
+ *     W_down (exact for every bf16 weight of magnitude 2^-14 .. 65504); an
+ *     |h| or |y| above 65504 is reported as MOE_ERR_NONFINITE (diagnostic
+ *     word 1 = 5 for h, 6 for y).  With MOE_FLAG_DOWN_HILO h is instead kept
+ *     as a bf16 hi/lo pair against the bf16 W_down and y in fp32 (no range
  *     limit, twice the down-GEMM work).  Either way the layer stays within
  *     1e-2 of the output rms; fp32 or bf16 output.
  *   MOE_FP8_E4M3_B128: expert weights as E4M3 codes with one fp32 scale per
@@ -147,11 +148,13 @@ typedef struct moe_ws_layout {
     size_t xq_scale;   /* FP8: f32 [T, D/128] */
     size_t xp;         /* [T*top_k, D] x gathered into grouped order (layer dtype; E4M3 for FP8) */
     size_t xp_scale;   /* FP8: f32 [T*top_k, D/128] */
-    size_t h;          /* SwiGLU activations: f32 [R, I] | bf16 hi/lo pair [R, 2I] (hi in
+    size_t h;          /* SwiGLU activations: f32 [R, I] (MOE_F32) | fp16 [R, I] (MOE_BF16) |
+                          bf16 hi/lo pair [R, 2I] (MOE_BF16 + MOE_FLAG_DOWN_HILO: hi in
                           columns 0..I-1, lo = bf16(h - hi) in I..2I-1) | E4M3 [R, I];
                           R = T*top_k + T */
     size_t h_scale;    /* FP8: f32 [T*top_k + T, I/128] */
-    size_t y;          /* [R, D] expert outputs: f32 (MOE_F32, MOE_BF16) or bf16 (FP8 layer) */
+    size_t y;          /* [R, D] expert outputs: f32 (MOE_F32; MOE_BF16 + MOE_FLAG_DOWN_HILO),
+                          fp16 (MOE_BF16) or bf16 (FP8 layer) */
     size_t logits_part;/* f32 [S, T, E] router K-slice partials when T is small (S > 1), else 0 */
     size_t tiles2;     /* int32 [E+2]: exclusive prefix of ceil(counts/256) (row-tile pairs) */
 } moe_ws_layout;

@@ -47,6 +47,10 @@ size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 // else h as one fp16 against an fp16 copy of W_down.
 bool hilo(const moe_config& c) { return c.dtype == MOE_BF16 && (c.flags & MOE_FLAG_DOWN_HILO); }
 bool f16_down(const moe_config& c) { return c.dtype == MOE_BF16 && !(c.flags & MOE_FLAG_DOWN_HILO); }
+// Expert outputs y: bf16 (FP8 layer), fp16 (bf16 layer, fp16 down path), else fp32.
+int y_elem(const moe_config& c) {
+    return c.dtype == MOE_FP8_E4M3_B128 ? moe::kBF16 : f16_down(c) ? moe::kF16 : moe::kF32;
+}
 
 int act_bytes(int dtype) { return dtype == MOE_F32 ? 4 : (dtype == MOE_BF16 ? 2 : 1); }
 int act_elem(int dtype) { return dtype == MOE_F32 ? moe::kF32 : (dtype == MOE_BF16 ? moe::kBF16 : moe::kE4M3); }
@@ -84,7 +88,7 @@ void layout(const moe_config& c, int num_sms, int T, moe_ws_layout* L) {
     L->h_scale = fp8 ? take((size_t)R * (c.I / 128) * 4) : 0;
     // y in fp32 except for the FP8 layer (bf16 there): a bf16 y alone costs
     // about 1.3e-2 of the output rms, above the bf16 layer's tolerance.
-    L->y = take((size_t)R * c.D * (c.dtype == MOE_FP8_E4M3_B128 ? 2 : 4));
+    L->y = take((size_t)R * c.D * (y_elem(c) == moe::kF32 ? 4 : 2));
     const int S = route_splits(c, T, num_sms);
     L->logits_part = S > 1 ? take((size_t)S * T * c.E * 4) : 0;
     L->tiles2 = take((size_t)(c.E + 2) * 4);
@@ -418,7 +422,7 @@ moe_status moe_gemm_down(const moe_plan* p, const moe_weights* w, int32_t T, voi
     }
     g.b_scale = w->s_down;
     g.out = W.at<void>(W.L.y);
-    g.out_elem = fp8 ? moe::kBF16 : moe::kF32;
+    g.out_elem = y_elem(c);
     g.err = W.at<uint32_t>(W.L.err);
     g.spin_ns = p->spin_ns;
     return run_gemm(p, g, (cudaStream_t)stream, "down GEMM");
@@ -430,7 +434,7 @@ moe_status moe_unpermute(const moe_plan* p, int32_t T, void* out, void* ws, size
     if (st != MOE_OK) return st;
     if (!ptr_ok(out)) return arg_fail(MOE_ERR_INVALID_ARG, "out NULL or misaligned");
     const moe_config& c = p->cfg;
-    MOE_CUDA(moe::launch_unpermute(W.at<void>(W.L.y), c.dtype == MOE_FP8_E4M3_B128 ? moe::kBF16 : moe::kF32,
+    MOE_CUDA(moe::launch_unpermute(W.at<void>(W.L.y), y_elem(c),
                                    W.at<int32_t>(W.L.blob), W.at<int32_t>(W.L.inv), T, c.D, c.top_k, out,
                                    c.out_dtype == MOE_F32 ? moe::kF32 : moe::kBF16, W.at<uint32_t>(W.L.err),
                                    (cudaStream_t)stream));

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(GroupedGemm g) {
                 if (g.bias) v += __ldg(g.bias + n);
                 const int64_t o = (int64_t)(out0 + m) * g.ldo + n;
                 if (std::is_same<TO, f16>::value && !(fabsf(v) <= 65504.f))
-                    record_error(g.err, MOE_ERR_NONFINITE, 5, blockIdx.x, 1);
+                    record_error(g.err, MOE_ERR_NONFINITE, SWIGLU ? 5 : 6, blockIdx.x, 1);
                 const TO hi = from_f32<TO>(v);
                 out[o] = hi;
                 if (g.out_pair) out[o + N] = from_f32<TO>(v - to_f32(hi));
@@ -158,6 +158,9 @@ cudaError_t launch_gemm_simt(const GroupedGemm& g, cudaStream_t stream) {
     else if (g.elem == kBF16 && be == kBF16 && g.out_elem == kBF16) MOE_SIMT(bf16, bf16, bf16);
     else if (g.elem == kBF16 && be == kBF16 && g.out_elem == kF16) MOE_SIMT(bf16, bf16, f16);
     else if (g.elem == kF16 && be == kBF16 && g.out_elem == kF32) MOE_SIMT(f16, bf16, float);
+    else if (g.elem == kF16 && be == kBF16 && g.out_elem == kF16) MOE_SIMT(f16, bf16, f16);
+    else if (g.elem == kF16 && be == kF16 && g.out_elem == kF32) MOE_SIMT(f16, f16, float);
+    else if (g.elem == kF16 && be == kF16 && g.out_elem == kF16) MOE_SIMT(f16, f16, f16);
     else return cudaErrorInvalidValue;
 #undef MOE_SIMT
     count_launches(1);

@@ -373,7 +373,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             float v[32];
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-                            store_bf16x32((bf16*)p.out + orow * p.ldo + n0, v);
+                            if (p.out_f16) {
+                                float m = 0.f;
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) m = fmaxf(m, fabsf(v[i]));
+                                if (!(m <= 65504.f)) record_error(p.err, MOE_ERR_NONFINITE, 6, blockIdx.x, 0);
+                                store_f16x32((f16*)p.out + orow * p.ldo + n0, v);
+                            } else {
+                                store_bf16x32((bf16*)p.out + orow * p.ldo + n0, v);
+                            }
                         }
                     }
                 }
@@ -469,7 +477,7 @@ bool gemm_tc_supported(const GroupedGemm& g) {
         if (!aligned16(g.b2) || (g.a_shared && !aligned16(g.a_shared))) return false;
     } else {
         if (!plain_bn(g.N) || g.out_pair) return false;
-        if (g.out_elem != kBF16 && g.out_elem != kF32) return false;
+        if (g.out_elem != kBF16 && g.out_elem != kF32 && g.out_elem != kF16) return false;
         if (g.bias && g.out_elem != kF32) return false;
     }
     if (g.ldo % 8) return false;

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const TY* __restrict__ y
         pb[1] = __floats2bfloat162_rn(acc[2], acc[3]);
         *(uint2*)o = p;
     } else {
-        static_assert(V == 8, "bf16 y carries 8 values per 16-byte vector");
+        static_assert(V == 8, "16-bit y carries 8 values per 16-byte vector");
         uint4 p;
         __nv_bfloat162* pb = (__nv_bfloat162*)&p;
 #pragma unroll
@@ -93,14 +93,17 @@ cudaError_t launch_unpermute(const void* y, int y_elem, const int32_t* blob, con
     const int vecs = D / V;
     const int threads = std::min(256, ((vecs + 31) / 32) * 32);
     dim3 grid((unsigned)T, (unsigned)cdiv(vecs, threads));
-    if (y_elem == kF32 && out_elem == kF32)
-        unpermute_kernel<float, float><<<grid, threads, 0, stream>>>((const float*)y, blob, inv, T, D, k, (float*)out, err);
-    else if (y_elem == kF32)
-        unpermute_kernel<float, bf16><<<grid, threads, 0, stream>>>((const float*)y, blob, inv, T, D, k, (bf16*)out, err);
-    else if (out_elem == kF32)
-        unpermute_kernel<bf16, float><<<grid, threads, 0, stream>>>((const bf16*)y, blob, inv, T, D, k, (float*)out, err);
-    else
-        unpermute_kernel<bf16, bf16><<<grid, threads, 0, stream>>>((const bf16*)y, blob, inv, T, D, k, (bf16*)out, err);
+#define MOE_UNPERMUTE(TY, TO) \
+    unpermute_kernel<TY, TO><<<grid, threads, 0, stream>>>((const TY*)y, blob, inv, T, D, k, (TO*)out, err)
+    const bool o32 = out_elem == kF32;
+    if (y_elem == kF32) {
+        if (o32) MOE_UNPERMUTE(float, float); else MOE_UNPERMUTE(float, bf16);
+    } else if (y_elem == kF16) {
+        if (o32) MOE_UNPERMUTE(f16, float); else MOE_UNPERMUTE(f16, bf16);
+    } else {
+        if (o32) MOE_UNPERMUTE(bf16, float); else MOE_UNPERMUTE(bf16, bf16);
+    }
+#undef MOE_UNPERMUTE
     count_launches(1);
     return cudaGetLastError();
 }

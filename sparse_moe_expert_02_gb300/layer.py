@@ -122,9 +122,10 @@ class MoELayer:
         k, E, D, I = self.top_k, self.E, self.D, self.I
         TK, R = T * k, T * k + T
         act = {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.uint8}[self.dtype]
-        ydt = torch.bfloat16 if self.dtype == "fp8" else torch.float32
+        f16_down = self.dtype == "bf16" and not self.hilo
+        ydt = torch.bfloat16 if self.dtype == "fp8" else torch.float16 if f16_down else torch.float32
         hcols = 2 * I if self.hilo else I
-        hdt = torch.float16 if self.dtype == "bf16" and not self.hilo else act
+        hdt = torch.float16 if f16_down else act
         v = {
             "err": self.ws_view(T, "err", torch.int32, (4,)),
             "logits": self.ws_view(T, "logits", torch.float32, (T, E)),
