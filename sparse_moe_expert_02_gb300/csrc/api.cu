@@ -81,13 +81,13 @@ void layout(const moe_config& c, int num_sms, int T, moe_ws_layout* L) {
     L->xq_scale = fp8 ? take((size_t)T * (c.D / 128) * 4) : 0;
     L->xp = take((size_t)TK * c.D * ab);
     L->xp_scale = fp8 ? take((size_t)TK * (c.D / 128) * 4) : 0;
-    // bf16 layer: h is a bf16 hi/lo pair per element ([R, 2I]); the pair
-    // keeps the down GEMM's input at ~fp32 precision (a single bf16 rounding
-    // of h alone costs about 1e-2 of the output rms).
+    // bf16 layer: h in fp16 ([R, I]), or as a bf16 hi/lo pair ([R, 2I]) under
+    // MOE_FLAG_DOWN_HILO; a single bf16 rounding of h alone would cost about
+    // 1e-2 of the output rms.
     L->h = take((size_t)R * c.I * (hilo(c) ? 4 : ab));
     L->h_scale = fp8 ? take((size_t)R * (c.I / 128) * 4) : 0;
-    // y in fp32 except for the FP8 layer (bf16 there): a bf16 y alone costs
-    // about 1.3e-2 of the output rms, above the bf16 layer's tolerance.
+    // y: fp16 for the bf16 layer, bf16 for the FP8 layer, else fp32 (a bf16 y
+    // in the bf16 layer would cost about 1.3e-2 of the output rms).
     L->y = take((size_t)R * c.D * (y_elem(c) == moe::kF32 ? 4 : 2));
     const int S = route_splits(c, T, num_sms);
     L->logits_part = S > 1 ? take((size_t)S * T * c.E * 4) : 0;
