@@ -52,10 +52,13 @@ constexpr uint32_t kSmemBytes = 1024 + 196608 + 256;
 // Stage geometry.  PAIR: A is a bf16 hi/lo pair (hi in columns [0, Kb), lo in
 // [Kb, 2Kb)); a stage holds the hi and lo tiles of one k-block next to one B
 // tile, so the weights stream once and both halves multiply the same tile.
+// The ring holds as many stages of A + B as fit in kRingBytes (at most
+// kMaxStages): 4 for 256-wide B tiles, 6 for 128-wide, 8 for narrower.
+constexpr int kRingBytes = 196608;
+constexpr int kMaxStages = 8;
 template <bool PAIR> struct Geo {
-    static constexpr int kStages = PAIR ? 3 : 4;
     static constexpr int kAStage = PAIR ? 2 * kABytes : kABytes;
-    static_assert(kStages * (kAStage + kBBytesMax) <= 196608, "stage ring exceeds the smem budget");
+    static_assert(3 * (kAStage + kBBytesMax) <= kRingBytes, "stage ring exceeds the smem budget");
 };
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_PLAIN = 1 };
@@ -78,6 +81,8 @@ struct Params {
     int out_f32;
     int out_f16;         // SwiGLU output as fp16 (single rounding) instead of bf16
     int in_f16;          // A and B are fp16 (else bf16)
+    int stages;          // ring depth (<= kMaxStages)
+    int b_stage;         // bytes of one B stage
     void* out;
     const float* bias;
     uint32_t* err;
@@ -144,11 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    constexpr int kStages = Geo<PAIR>::kStages;
+    const int kStages = p.stages;
+    const int kBStage = p.b_stage;
     constexpr int kAStage = Geo<PAIR>::kAStage;
     uint8_t* sA = smem;
     uint8_t* sB = smem + kStages * kAStage;
-    uint64_t* bars = (uint64_t*)(sB + kStages * kBBytesMax);
+    uint64_t* bars = (uint64_t*)(smem + kRingBytes);
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
     const uint32_t tfull0 = smem_u32(bars + 2 * kStages), tempty0 = smem_u32(bars + 2 * kStages + 2);
     const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
@@ -214,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     armed |= 1u << stage;
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     const uint32_t a_dst = smem_u32(sA + stage * kAStage);
-                    const uint32_t b_dst = smem_u32(sB + stage * kBBytesMax);
+                    const uint32_t b_dst = smem_u32(sB + stage * kBStage);
                     if (nbox * kBoxRowsA == BM) {  // (nearly) full tile: one 128-row box
                         tma_load_2d(a_dst, taf, fb, kb * BK, a_y);
                         if (PAIR) tma_load_2d(a_dst + kABytes, taf, fb, p.a_lo_x + kb * BK, a_y);
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const uint64_t ad = umma_desc(smem_u32(sA + stage * kAStage));
-                    const uint64_t bd = umma_desc(smem_u32(sB + stage * kBBytesMax));
+                    const uint64_t bd = umma_desc(smem_u32(sB + stage * kBStage));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)  // K=16 per MMA: 32 bytes along the swizzled row
                         umma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
@@ -516,6 +522,8 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     p.out_f32 = g.out_elem == kF32;
     p.out_f16 = g.out_elem == kF16;
     p.in_f16 = g.elem == kF16;
+    p.b_stage = (sw ? 256 : p.BN) * BK * 2;
+    p.stages = std::min(kMaxStages, kRingBytes / ((pair ? Geo<true>::kAStage : Geo<false>::kAStage) + p.b_stage));
     p.out = g.out;
     p.bias = g.bias;
     p.err = g.err;

@@ -66,15 +66,31 @@ __device__ void warp_exclusive_scan(const int32_t* v, int n, int32_t* out) {
 
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E, int T,
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                                                         int32_t* __restrict__ tiles, int32_t* __restrict__ tiles2) {
+                                                         int32_t* __restrict__ tiles, int32_t* __restrict__ tiles2,
+                                                         int32_t* __restrict__ shared_src, int64_t TK) {
     __shared__ int32_t cnt[1025 + 1];
     __shared__ int32_t ntile[1025 + 1];
     __shared__ int32_t ntile2[1025 + 1];
+    // the shared expert's rows: token t at grouped row T*k + t
+    for (int t = threadIdx.x; t < T; t += blockDim.x) shared_src[TK + t] = t;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        // 8 independent loads in flight per step of the running sum
+        constexpr int U = 8;
         int run = 0;
-        for (int c = 0; c < nchunks; ++c) {
-            int64_t i = (int64_t)c * E + e;
-            int v = hist[i];
+        int c = 0;
+        for (; c + U <= nchunks; c += U) {
+            int v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) v[u] = hist[(int64_t)(c + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                hist[(int64_t)(c + u) * E + e] = run;
+                run += v[u];
+            }
+        }
+        for (; c < nchunks; ++c) {
+            const int64_t i = (int64_t)c * E + e;
+            const int v = hist[i];
             hist[i] = run;
             run += v;
         }
@@ -104,13 +120,22 @@ __global__ void __launch_bounds__(32) perm_rank_kernel(const int32_t* __restrict
     const int lane = threadIdx.x;
     const int chunk = perm_chunk(TK);
     const int64_t a0 = (int64_t)blockIdx.x * chunk;
+    // the chunk's expert ids, all loaded before the walk (chunk <= 32 * 32)
+    int ids[kPermChunk / 32];
+#pragma unroll
+    for (int s = 0; s < kPermChunk / 32; ++s) {
+        const int64_t a = a0 + 32 * s + lane;
+        ids[s] = (32 * s < chunk && a < TK) ? __ldg(idx + a) : -1;
+    }
     for (int e = lane; e < E; e += 32) cursor[e] = __ldg(offsets + e) + __ldg(hist + (int64_t)blockIdx.x * E + e);
     __syncwarp();
     const unsigned lt = (1u << lane) - 1u;
-    for (int s = 0; s < chunk; s += 32) {
+#pragma unroll
+    for (int si = 0; si < kPermChunk / 32; ++si) {
+        const int s = 32 * si;
+        if (s >= chunk) break;
         const int64_t a = a0 + s + lane;
-        const bool valid = a < TK;
-        int e = valid ? __ldg(idx + a) : -1;
+        int e = ids[si];
         if ((unsigned)e >= (unsigned)E) e = -1;  // out-of-range ids were reported by hist
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         int pos = 0;
@@ -207,10 +232,6 @@ __global__ void __launch_bounds__(1024) perm_index_small_kernel(const int32_t* _
     }
 }
 
-__global__ void shared_rows_kernel(int32_t* __restrict__ src_tok, int64_t TK, int T) {
-    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += gridDim.x * blockDim.x) src_tok[TK + t] = t;
-}
-
 cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_t* hist, int32_t* counts,
                                  int32_t* offsets, int32_t* tiles, int32_t* tiles2, int32_t* inv, int32_t* src_tok,
                                  uint32_t* err, cudaStream_t stream) {
@@ -231,10 +252,9 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
     }
     const int nch = (int)cdiv(TK, perm_chunk(TK));
     perm_hist_kernel<<<nch, 256, E * sizeof(int32_t), stream>>>(idx, TK, E, hist, err);
-    perm_scan_kernel<<<1, 1024, 0, stream>>>(hist, nch, E, T, counts, offsets, tiles, tiles2);
+    perm_scan_kernel<<<1, 1024, 0, stream>>>(hist, nch, E, T, counts, offsets, tiles, tiles2, src_tok, TK);
     perm_rank_kernel<<<nch, 32, E * sizeof(int32_t), stream>>>(idx, TK, k, E, hist, offsets, inv, src_tok);
-    shared_rows_kernel<<<(unsigned)cdiv(T, 256), 256, 0, stream>>>(src_tok, TK, T);
-    count_launches(4);
+    count_launches(3);
     return cudaGetLastError();
 }
 
@@ -251,7 +271,15 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const V* __restrict__ 
     for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
         const V* src = x + (int64_t)__ldg(src_tok + r) * row_vecs;
         V* dst = xp + (int64_t)r * row_vecs;
-        for (int64_t i = lane; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
+        int64_t i = lane;
+        for (; i + 32 * 7 < row_vecs; i += 32 * 8) {  // 8 independent loads per lane in flight
+            V t[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) t[u] = __ldg(src + i + 32 * u);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) dst[i + 32 * u] = t[u];
+        }
+        for (; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
     }
 }
 
