@@ -63,6 +63,16 @@ __host__ __device__ constexpr int64_t cdiv(int64_t a, int64_t b) { return (a + b
 
 // Group of a row tile: tiles[g] <= tile < tiles[g+1] (tiles has G+1 entries,
 // nondecreasing).  Binary search, G <= 1025.
+// The same over a copy of the prefix in shared memory.
+__device__ __forceinline__ int find_group_smem(const int32_t* tiles, int G, int tile) {
+    int lo = 0, hi = G;
+    while (hi - lo > 1) {
+        int mid = (lo + hi) >> 1;
+        if (tiles[mid] <= tile) lo = mid;
+        else hi = mid;
+    }
+    return lo;
+}
 __device__ __forceinline__ int find_group(const int32_t* tiles, int G, int tile) {
     int lo = 0, hi = G;  // invariant: tiles[lo] <= tile < tiles[hi]
     while (hi - lo > 1) {

@@ -47,7 +47,10 @@ constexpr int kAccCols = 256;             // TMEM columns per accumulator buffer
 constexpr int kBoxRowsA = 16;             // a ragged tile's A rows come in 16-row boxes (2 KB);
                                           // a full tile's in one 128-row box: the single
                                           // producer thread issues few TMA instructions
-constexpr uint32_t kSmemBytes = 1024 + 196608 + 256;
+// Shared-memory copy of the group row-tile prefix and row offsets (G <= 1025
+// groups): a unit's group comes from a binary search that never leaves the SM.
+constexpr int kTabEntries = 1056;
+constexpr uint32_t kSmemBytes = 1024 + 196608 + 256 + 2 * kTabEntries * 4;
 
 // Stage geometry.  PAIR: A is a bf16 hi/lo pair (hi in columns [0, Kb), lo in
 // [Kb, 2Kb)); a stage holds the hi and lo tiles of one k-block next to one B
@@ -95,8 +98,10 @@ struct Unit {
     int g, m0, row0, nrows, nb, ks;
 };
 
-// Units: K slice major, then row tile, then feature block.
-__device__ __forceinline__ Unit decode_unit(const Params& p, int u, int total_tiles) {
+// Units: K slice major, then row tile, then feature block.  s_tiles/s_off:
+// shared copies of p.tiles and p.offsets (entries 0..G).
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u, int total_tiles, const int32_t* s_tiles,
+                                            const int32_t* s_off) {
     Unit r;
     const int per_slice = total_tiles * p.NB;
     r.ks = u / per_slice;
@@ -104,10 +109,10 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u, int total_ti
     const int rt = u / p.NB;
     r.nb = u - rt * p.NB;
     if (p.offsets) {
-        r.g = find_group(p.tiles, p.G, rt);
-        r.m0 = (rt - __ldg(p.tiles + r.g)) * BM;
-        r.row0 = __ldg(p.offsets + r.g);
-        r.nrows = __ldg(p.offsets + r.g + 1) - r.row0;
+        r.g = find_group_smem(s_tiles, p.G, rt);
+        r.m0 = (rt - s_tiles[r.g]) * BM;
+        r.row0 = s_off[r.g];
+        r.nrows = s_off[r.g + 1] - r.row0;
     } else {
         r.g = 0;
         r.m0 = rt * BM;
@@ -155,6 +160,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sA = smem;
     uint8_t* sB = smem + kStages * kAStage;
     uint64_t* bars = (uint64_t*)(smem + kRingBytes);
+    int32_t* s_tiles = (int32_t*)(smem + kRingBytes + 256);
+    int32_t* s_off = s_tiles + kTabEntries;
+    if (p.offsets)
+        for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
+            s_tiles[i] = __ldg(p.tiles + i);
+            s_off[i] = __ldg(p.offsets + i);
+        }
     const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
     const uint32_t tfull0 = smem_u32(bars + 2 * kStages), tempty0 = smem_u32(bars + 2 * kStages + 2);
     const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
@@ -199,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b_bytes = (EPI == EPI_SWIGLU) ? 2u * 128 * BK * 2 : (uint32_t)p.BN * BK * 2;
             bool ok = true;
             for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-                const Unit un = decode_unit(p, u, total_tiles);
+                const Unit un = decode_unit(p, u, total_tiles, s_tiles, s_off);
                 const bool sh = un.g == p.shared_group;
                 const CUtensorMap* ta = sh ? &tm_a_sh : &tm_a;
                 const CUtensorMap* taf = sh ? &tm_a_shf : &tm_af;
@@ -309,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
-            const Unit un = decode_unit(p, u, total_tiles);
+            const Unit un = decode_unit(p, u, total_tiles, s_tiles, s_off);
             int ok = 1;
             if (lane == 0) {
                 ok = mbar_wait(tfull0 + 8 * acc, acc_phase, lim, abort_flag);
@@ -474,6 +486,7 @@ bool gemm_tc_supported(const GroupedGemm& g) {
     if (g.elem != kBF16 && g.elem != kF16) return false;
     if (g.b_elem > 0 && g.b_elem != g.elem) return false;  // the tensor cores take one type for A and B
     if (!encode_fn()) return false;
+    if (g.offsets && g.G + 1 > kTabEntries) return false;
     if (g.Kb % BK || g.Kb < BK || (g.Ka != g.Kb && g.Ka != 2 * g.Kb)) return false;
     if (g.b2 && g.Ka != g.Kb) return false;  // the hi/lo pair is only the down GEMM's input
     if (!aligned16(g.a) || !aligned16(g.b) || !aligned16(g.out)) return false;
