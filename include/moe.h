@@ -162,7 +162,8 @@ typedef struct moe_ws_layout {
 /* Validate a configuration and build a host-side plan for `device`.
  * Supported: D, I multiples of 128 (64 for MOE_F32), E <= 1024,
  * 1 <= top_k <= min(E, 32), 1 <= T_max <= 2^20, T_max*(top_k+1) < 2^31.
- * The plan owns no device memory.  *out is NULL on error. */
+ * The plan owns no device memory; it holds one CUDA stream and two events
+ * on `device` (see moe_forward).  *out is NULL on error. */
 MOE_API moe_status moe_plan_create(const moe_config* cfg, int device, moe_plan** out);
 MOE_API void moe_plan_destroy(moe_plan* plan);
 MOE_API const moe_config* moe_plan_config(const moe_plan* plan);
@@ -186,7 +187,14 @@ MOE_API moe_status moe_quantize_weights(const moe_plan* plan, const float* w, in
  * unpermute with the shared-expert add.  x [T, D] (fp32 for MOE_F32, else
  * bf16); out [T, D] of cfg.out_dtype.  blob_out (nullable) receives a copy of
  * the [2, T, top_k] routing blob; logits_out (nullable) a copy of the [T, E]
- * fp32 logits.  Clears the workspace error word first. */
+ * fp32 logits.  Clears the workspace error word first.
+ * On the bf16 tensor-core path (not MOE_FLAG_FORCE_SIMT or
+ * MOE_FLAG_PAIR_CTA_ON) the shared expert's two GEMMs, which need no
+ * routing, run on the plan's own stream, forked from `stream` with an event
+ * at the start and joined back before the unpermute, so they overlap the
+ * router, top-k and permutation; the call stays asynchronous and can be
+ * captured into a CUDA graph.  A plan must therefore not be used by two host
+ * threads calling moe_forward at the same time. */
 MOE_API moe_status moe_forward(const moe_plan* plan, const moe_weights* w, const void* x, int32_t T, void* out,
                        int32_t* blob_out, float* logits_out, void* ws, size_t ws_bytes, void* stream);
 

@@ -20,6 +20,10 @@ struct moe_plan {
     int device;
     int num_sms;
     int64_t spin_ns;
+    // moe_forward runs the shared expert on a second stream, forked from and
+    // joined back into the caller's stream with these events
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
 };
 
 namespace {
@@ -227,11 +231,28 @@ moe_status moe_plan_create(const moe_config* cfg, int device, moe_plan** out) {
     p->device = device;
     p->num_sms = sms;
     p->spin_ns = c.spin_limit_ns ? c.spin_limit_ns : 2000000000LL;
+    int prev = 0;
+    cudaGetDevice(&prev);
+    if (cudaSetDevice(device) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+        moe_plan_destroy(p);
+        cudaSetDevice(prev);
+        return arg_fail(MOE_ERR_CUDA, "stream or event creation failed");
+    }
+    cudaSetDevice(prev);
     *out = p;
     return MOE_OK;
 }
 
-void moe_plan_destroy(moe_plan* p) { delete p; }
+void moe_plan_destroy(moe_plan* p) {
+    if (!p) return;
+    if (p->ev_fork) cudaEventDestroy(p->ev_fork);
+    if (p->ev_join) cudaEventDestroy(p->ev_join);
+    if (p->side) cudaStreamDestroy(p->side);
+    delete p;
+}
 
 const moe_config* moe_plan_config(const moe_plan* p) { return p ? &p->cfg : nullptr; }
 
@@ -348,13 +369,9 @@ moe_status moe_permute(const moe_plan* p, const void* x, int32_t T, void* ws, si
     return MOE_OK;
 }
 
-moe_status moe_gemm_gateup(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, void* ws,
-                           size_t ws_bytes, void* stream) {
-    Ws W;
-    moe_status st = check_call(p, T, ws, ws_bytes, &W);
-    if (st != MOE_OK) return st;
-    if ((st = check_weights(p, w, false, true)) != MOE_OK) return st;
-    if (!ptr_ok(x)) return arg_fail(MOE_ERR_INVALID_ARG, "x NULL or misaligned");
+namespace {
+
+moe::GroupedGemm gateup_gemm(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, Ws& W) {
     const moe_config& c = p->cfg;
     const bool fp8 = c.dtype == MOE_FP8_E4M3_B128;
     moe::GroupedGemm g = {};
@@ -386,15 +403,10 @@ moe_status moe_gemm_gateup(const moe_plan* p, const moe_weights* w, const void* 
     g.out_scale = fp8 ? W.at<float>(W.L.h_scale) : nullptr;
     g.err = W.at<uint32_t>(W.L.err);
     g.spin_ns = p->spin_ns;
-    return run_gemm(p, g, (cudaStream_t)stream, "gate/up GEMM");
+    return g;
 }
 
-moe_status moe_gemm_down(const moe_plan* p, const moe_weights* w, int32_t T, void* ws, size_t ws_bytes,
-                         void* stream) {
-    Ws W;
-    moe_status st = check_call(p, T, ws, ws_bytes, &W);
-    if (st != MOE_OK) return st;
-    if ((st = check_weights(p, w, false, true)) != MOE_OK) return st;
+moe::GroupedGemm down_gemm(const moe_plan* p, const moe_weights* w, int32_t T, Ws& W) {
     const moe_config& c = p->cfg;
     const bool fp8 = c.dtype == MOE_FP8_E4M3_B128;
     moe::GroupedGemm g = {};
@@ -425,7 +437,57 @@ moe_status moe_gemm_down(const moe_plan* p, const moe_weights* w, int32_t T, voi
     g.out_elem = y_elem(c);
     g.err = W.at<uint32_t>(W.L.err);
     g.spin_ns = p->spin_ns;
-    return run_gemm(p, g, (cudaStream_t)stream, "down GEMM");
+    return g;
+}
+
+int elem_bytes(int e) { return e == moe::kF32 ? 4 : e == moe::kE4M3 ? 1 : 2; }
+
+// The shared expert alone, as a dense GEMM over its T rows (which sit after
+// the T*k routed rows of the grouped layout).  Its A comes from x (gate/up)
+// or from the shared rows of h (down); its B is group E of the weights.
+moe::GroupedGemm shared_only(const moe::GroupedGemm& full, const moe_config& c, int32_t T, bool gateup,
+                             const void* x) {
+    moe::GroupedGemm g = full;
+    const int64_t TK = (int64_t)T * c.top_k;
+    g.G = 1;
+    g.shared_group = -1;
+    g.offsets = g.tiles = g.tiles2 = nullptr;
+    g.prefer_pairs = 0;
+    g.rows = T;
+    g.max_tiles = (int)moe::cdiv(T, moe::kRowTile);
+    g.a_rows = T;
+    g.a_shared = nullptr;
+    g.a_shared_rows = 0;
+    const int eb = elem_bytes(g.elem);
+    const int bb = elem_bytes(g.b_elem > 0 ? g.b_elem : g.elem);
+    if (gateup) g.a = x;
+    else g.a = (const char*)full.a + TK * g.Ka * eb;
+    const int64_t group = (int64_t)g.N * g.Kb * bb;
+    g.b = (const char*)full.b + c.E * group;
+    if (g.b2) g.b2 = (const char*)full.b2 + c.E * group;
+    g.out = (char*)full.out + TK * g.ldo * elem_bytes(g.out_elem);
+    return g;
+}
+
+}  // namespace
+
+moe_status moe_gemm_gateup(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, void* ws,
+                           size_t ws_bytes, void* stream) {
+    Ws W;
+    moe_status st = check_call(p, T, ws, ws_bytes, &W);
+    if (st != MOE_OK) return st;
+    if ((st = check_weights(p, w, false, true)) != MOE_OK) return st;
+    if (!ptr_ok(x)) return arg_fail(MOE_ERR_INVALID_ARG, "x NULL or misaligned");
+    return run_gemm(p, gateup_gemm(p, w, x, T, W), (cudaStream_t)stream, "gate/up GEMM");
+}
+
+moe_status moe_gemm_down(const moe_plan* p, const moe_weights* w, int32_t T, void* ws, size_t ws_bytes,
+                         void* stream) {
+    Ws W;
+    moe_status st = check_call(p, T, ws, ws_bytes, &W);
+    if (st != MOE_OK) return st;
+    if ((st = check_weights(p, w, false, true)) != MOE_OK) return st;
+    return run_gemm(p, down_gemm(p, w, T, W), (cudaStream_t)stream, "down GEMM");
 }
 
 moe_status moe_unpermute(const moe_plan* p, int32_t T, void* out, void* ws, size_t ws_bytes, void* stream) {
@@ -451,13 +513,38 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
     if ((blob_out && !aligned(blob_out, 16)) || (logits_out && !aligned(logits_out, 16)))
         return arg_fail(MOE_ERR_INVALID_ARG, "blob_out or logits_out misaligned");
     cudaStream_t s = (cudaStream_t)stream;
+    const moe_config& cf = p->cfg;
     MOE_CUDA(cudaMemsetAsync(ws, 0, 16, s));
-    if ((st = moe_route(p, w, x, T, ws, ws_bytes, stream)) != MOE_OK) return st;
-    if ((st = moe_permute(p, x, T, ws, ws_bytes, stream)) != MOE_OK) return st;
-    if ((st = moe_gemm_gateup(p, w, x, T, ws, ws_bytes, stream)) != MOE_OK) return st;
-    if ((st = moe_gemm_down(p, w, T, ws, ws_bytes, stream)) != MOE_OK) return st;
+    moe::GroupedGemm gu = gateup_gemm(p, w, x, T, W), dn = down_gemm(p, w, T, W);
+    const moe::GroupedGemm sgu = shared_only(gu, cf, T, true, x), sdn = shared_only(dn, cf, T, false, x);
+    // The shared expert needs no routing: on the tensor-core path its two
+    // GEMMs run on the plan's second stream while the router, top-k and
+    // permutation run here; the routed GEMMs then skip the shared group.
+    const bool overlap = cf.dtype == MOE_BF16 && !(cf.flags & MOE_FLAG_FORCE_SIMT) && !gu.prefer_pairs &&
+                         moe::gemm_tc_supported(gu) && moe::gemm_tc_supported(dn) &&
+                         moe::gemm_tc_supported(sgu) && moe::gemm_tc_supported(sdn);
+    if (overlap) {
+        gu.g_end = dn.g_end = cf.E;
+        MOE_CUDA(cudaEventRecord(p->ev_fork, s));
+        MOE_CUDA(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
+        moe_status side_st = run_gemm(p, sgu, p->side, "shared gate/up GEMM");
+        if (side_st == MOE_OK) side_st = run_gemm(p, sdn, p->side, "shared down GEMM");
+        MOE_CUDA(cudaEventRecord(p->ev_join, p->side));
+        st = moe_route(p, w, x, T, ws, ws_bytes, stream);
+        if (st == MOE_OK) st = moe_permute(p, x, T, ws, ws_bytes, stream);
+        if (st == MOE_OK) st = run_gemm(p, gu, s, "gate/up GEMM");
+        if (st == MOE_OK) st = run_gemm(p, dn, s, "down GEMM");
+        MOE_CUDA(cudaStreamWaitEvent(s, p->ev_join, 0));  // joined even after an error (stream capture)
+        if (side_st != MOE_OK) return side_st;
+        if (st != MOE_OK) return st;
+    } else {
+        if ((st = moe_route(p, w, x, T, ws, ws_bytes, stream)) != MOE_OK) return st;
+        if ((st = moe_permute(p, x, T, ws, ws_bytes, stream)) != MOE_OK) return st;
+        if ((st = run_gemm(p, gu, s, "gate/up GEMM")) != MOE_OK) return st;
+        if ((st = run_gemm(p, dn, s, "down GEMM")) != MOE_OK) return st;
+    }
     if ((st = moe_unpermute(p, T, out, ws, ws_bytes, stream)) != MOE_OK) return st;
-    const moe_config& c = p->cfg;
+    const moe_config& c = cf;
     if (blob_out)
         MOE_CUDA(cudaMemcpyAsync(blob_out, W.at<int32_t>(W.L.blob), (size_t)2 * T * c.top_k * 4,
                                  cudaMemcpyDeviceToDevice, s));

@@ -68,6 +68,7 @@ enum Epi : int { EPI_SWIGLU = 0, EPI_PLAIN = 1 };
 
 struct Params {
     int G, shared_group;
+    int g_end;           // units cover the row tiles of groups [0, g_end)
     const int32_t* offsets;
     const int32_t* tiles;
     int rows;            // single-group row count (offsets == nullptr)
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int total_tiles = p.offsets ? __ldg(p.tiles + p.G) : (p.rows + BM - 1) / BM;
+    const int total_tiles = p.offsets ? __ldg(p.tiles + p.g_end) : (p.rows + BM - 1) / BM;
     const int total_units = total_tiles * p.NB * p.KS;
     const int kbs = p.KB / p.KS;  // k-blocks per unit
     const int64_t lim = p.spin_ns;
@@ -510,6 +511,7 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     const bool pair = g.Ka == 2 * g.Kb;
     Params p = {};
     p.G = g.offsets ? g.G : 1;
+    p.g_end = (g.offsets && g.g_end > 0 && g.g_end < g.G) ? g.g_end : p.G;
     p.shared_group = g.shared_group;
     p.offsets = g.offsets;
     p.tiles = g.tiles;
