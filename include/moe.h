@@ -135,7 +135,10 @@ typedef struct moe_plan moe_plan;
  * grouped by expert), then the T rows of the shared expert. */
 typedef struct moe_ws_layout {
     size_t total;      /* bytes needed */
-    size_t err;        /* uint32[4]: first error code, then three diagnostic words */
+    size_t err;        /* uint32[4]: first error code, then three diagnostic words; the rest of
+                          this 256-byte block holds the GEMMs' unit-scheduling counters, which
+                          the kernels rewind themselves (moe_workspace_init and moe_forward
+                          zero the whole block) */
     size_t logits;     /* f32 [T, E] router logits (bias included) */
     size_t blob;       /* int32 [2, T, top_k]: expert index plane, fp32-weight-bits plane */
     size_t counts;     /* int32 [E+1]: rows per group; counts[E] = T */
@@ -172,7 +175,8 @@ MOE_API const moe_config* moe_plan_config(const moe_plan* plan);
 MOE_API moe_status moe_workspace_layout(const moe_plan* plan, int32_t T, moe_ws_layout* out);
 MOE_API moe_status moe_workspace_size(const moe_plan* plan, int32_t T, size_t* bytes);
 
-/* Zero the workspace's error word (moe_forward does this itself). */
+/* Zero the workspace's error word and scheduling counters (moe_forward does
+ * this itself; call it before stage entry points after an error). */
 MOE_API moe_status moe_workspace_init(const moe_plan* plan, void* ws, size_t ws_bytes, void* stream);
 
 /* Block-quantise fp32 weights to E4M3 (English page, "Roofline Validation":
@@ -188,7 +192,7 @@ MOE_API moe_status moe_quantize_weights(const moe_plan* plan, const float* w, in
  * bf16); out [T, D] of cfg.out_dtype.  blob_out (nullable) receives a copy of
  * the [2, T, top_k] routing blob; logits_out (nullable) a copy of the [T, E]
  * fp32 logits.  Clears the workspace error word first.
- * On the bf16 tensor-core path (not MOE_FLAG_FORCE_SIMT or
+ * On the tensor-core paths (bf16 and FP8; not MOE_FLAG_FORCE_SIMT or
  * MOE_FLAG_PAIR_CTA_ON) the shared expert's two GEMMs, which need no
  * routing, run on the plan's own stream, forked from `stream` with an event
  * at the start and joined back before the unpermute, so they overlap the

@@ -55,12 +55,16 @@ static_assert(4 * (kRegsLaunch - kRegsLow) == kEpiWarps * (kRegsHigh - kRegsLaun
 static_assert(kThreads * kRegsLaunch <= 65536, "launch registers exceed the SM");
 constexpr int kAccCols = 256;
 constexpr int kBoxRowsA = 16;
-constexpr uint32_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + 256 + 2 * 2 * 128 * 4;
+constexpr uint32_t kBarBytes = 512;  // mbarriers, TMEM address, abort flag, unit ring
+constexpr uint32_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + kBarBytes + 2 * 2 * 128 * 4;
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_PLAIN = 1 };
 
 struct Params {
     int G, shared_group;
+    int g_end;            // grouped: units cover the row tiles of groups [0, g_end)
+    int* sched;           // [2] device: next-unit counter and finished-CTA count, or nullptr (static order)
+    int rows;             // single group (offsets == nullptr): its row count
     const int32_t* offsets;
     const int32_t* tiles;
     int NB;               // feature blocks per row tile
@@ -85,10 +89,17 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
     Unit r;
     const int rt = u / p.NB;
     r.nb = u - rt * p.NB;
-    r.g = find_group(p.tiles, p.G, rt);
-    r.m0 = (rt - __ldg(p.tiles + r.g)) * BM;
-    r.row0 = __ldg(p.offsets + r.g);
-    r.nrows = __ldg(p.offsets + r.g + 1) - r.row0;
+    if (p.offsets) {
+        r.g = find_group(p.tiles, p.G, rt);
+        r.m0 = (rt - __ldg(p.tiles + r.g)) * BM;
+        r.row0 = __ldg(p.offsets + r.g);
+        r.nrows = __ldg(p.offsets + r.g + 1) - r.row0;
+    } else {
+        r.g = 0;
+        r.m0 = rt * BM;
+        r.row0 = 0;
+        r.nrows = p.rows;
+    }
     return r;
 }
 
@@ -109,9 +120,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // [2 unit parities][4 lane quarters]: amax exchange between the two warps
     // that hold the two column halves of the same 32 rows
     const uint32_t xbar0 = smem_u32(bars + 2 * kStages + 5);
-    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kStages + 13);
+    // unit ring: full/empty [4 each] and 4 slots (see gemm_tc.cu)
+    const uint32_t ufull0 = smem_u32(bars + 2 * kStages + 13), uempty0 = smem_u32(bars + 2 * kStages + 17);
+    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kStages + 21);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-    float* s_amax = (float*)(smem + kStages * (kABytes + kBBytes) + 256);  // [2 units][2 halves][128 rows]
+    volatile int* s_units = (volatile int*)(tmem_slot + 2);
+    static_assert((2 * kStages + 21) * 8 + 6 * 4 <= kBarBytes, "barrier block overflows");
+    float* s_amax = (float*)(smem + kStages * (kABytes + kBBytes) + kBarBytes);  // [2 units][2 halves][128 rows]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -125,6 +140,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(drain, 1);
         for (int b = 0; b < 8; ++b) mbar_init(xbar0 + 8 * b, 2 * 32);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(ufull0 + 8 * i, 1);
+            mbar_init(uempty0 + 8 * i, 1 + kEpiWarps);  // the MMA issuer and the epilogue warps
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -139,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int total_units = __ldg(p.tiles + p.G) * p.NB;
+    const int total_units = (p.offsets ? __ldg(p.tiles + p.g_end) : (p.rows + BM - 1) / BM) * p.NB;
     const int64_t lim = p.spin_ns;
 
     if (warp < kEpiWarp0) {
@@ -151,7 +170,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, armed = 0, armed_parity = 0;
             constexpr uint32_t b_bytes = 256u * BKB;
             bool ok = true;
-            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            // units from the launch-wide counter (drawn one ahead) or in the
+            // static round-robin order, published through the unit ring
+            int next_u = p.sched ? atomicAdd(p.sched, 1) : blockIdx.x;
+            for (int i = 0; ok; ++i) {
+                int u = next_u;
+                if (u >= total_units) u = -1;
+                if (u >= 0) next_u = p.sched ? atomicAdd(p.sched, 1) : blockIdx.x + (i + 1) * gridDim.x;
+                if (!mbar_wait(uempty0 + 8 * (i & 3), ((i >> 2) & 1) ^ 1, lim, abort_flag)) {
+                    record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 15, blockIdx.x, i);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                s_units[i & 3] = u;
+                mbar_arrive(ufull0 + 8 * (i & 3));
+                if (u < 0) break;
                 const Unit un = decode_unit(p, u);
                 const bool sh = un.g == p.shared_group;
                 const CUtensorMap* ta = sh ? &tm_a_sh : &tm_a;
@@ -203,7 +237,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, chunk = 0;
             const uint32_t idesc = idesc_e4m3(BM, 256);
             bool ok = true;
-            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            for (int i = 0; ok; ++i) {
+                if (!mbar_wait(ufull0 + 8 * (i & 3), (i >> 2) & 1, lim, abort_flag)) {
+                    record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 16, blockIdx.x, i);
+                    *abort_flag = 1;
+                    break;
+                }
+                const int u = s_units[i & 3];
+                mbar_arrive(uempty0 + 8 * (i & 3));
+                if (u < 0) break;
                 for (int kb = 0; kb < p.KB; ++kb) {
                     const uint32_t buf = chunk & 1u, cpar = (chunk >> 1) & 1u;
                     if (!mbar_wait(full0 + 8 * stage, phase, lim, abort_flag) ||
@@ -243,7 +285,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = sub * 32 + lane;
         uint32_t chunk = 0, nunit = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x, ++nunit) {
+        for (int i = 0; ok; ++i, ++nunit) {
+            int u = -1, got = 1;
+            if (lane == 0) {
+                got = mbar_wait(ufull0 + 8 * (i & 3), (i >> 2) & 1, lim, abort_flag);
+                if (got) {
+                    u = s_units[i & 3];
+                    mbar_arrive(uempty0 + 8 * (i & 3));
+                } else {
+                    record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 17, blockIdx.x, i);
+                    *abort_flag = 1;
+                }
+            }
+            got = __shfl_sync(0xffffffffu, got, 0);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (!got || u < 0) break;
             const int unit_par = nunit & 1;
             const Unit un = decode_unit(p, u);
             const bool sh = un.g == p.shared_group;
@@ -381,6 +437,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * kAccCols)
                      : "memory");
     }
+    if (p.sched && threadIdx.x == 0) {  // the last CTA rewinds the counters (see gemm_tc.cu)
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+            atomicExch(p.sched, 0);
+            atomicExch(p.sched + 1, 0);
+        }
+    }
 }
 
 bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
@@ -421,11 +484,13 @@ cudaError_t launch_one(int grid, const CUtensorMap& ma, const CUtensorMap& msh, 
 
 bool gemm_fp8_supported(const GroupedGemm& g) {
     using namespace tc::f8;
-    if (g.elem != kE4M3 || !g.offsets || !tc::encode_fn()) return false;
+    if (g.elem != kE4M3 || !tc::encode_fn()) return false;
+    if (!g.offsets && (g.rows < 1 || g.a_shared)) return false;  // single group: A only
     if (g.Ka != g.Kb || g.Kb % BKB || g.N % 128) return false;
     if (!g.a_scale || !g.b_scale) return false;
     if (g.b2) {
-        if (!g.b2_scale || !g.out_scale || g.out_elem != kE4M3 || !g.a_shared || !g.a_shared_scale) return false;
+        if (!g.b2_scale || !g.out_scale || g.out_elem != kE4M3) return false;
+        if (g.offsets && (!g.a_shared || !g.a_shared_scale)) return false;
     } else {
         if (g.N % 256 || g.out_elem != kBF16) return false;
     }
@@ -439,6 +504,10 @@ cudaError_t launch_gemm_fp8(const GroupedGemm& g, int num_sms, cudaStream_t stre
     p.G = g.G;
     p.shared_group = g.shared_group;
     p.offsets = g.offsets;
+    p.rows = g.rows;
+    p.sched = g.sched;
+    p.g_end = (g.offsets && g.g_end > 0 && g.g_end < g.G) ? g.g_end : g.G;
+    if (!g.offsets) p.G = 1;
     p.tiles = g.tiles;
     p.NB = sw ? g.N / 128 : g.N / 256;
     p.N = g.N;
@@ -470,7 +539,7 @@ cudaError_t launch_gemm_fp8(const GroupedGemm& g, int num_sms, cudaStream_t stre
     }
     const int max_units = g.max_tiles * p.NB;
     if (max_units <= 0) return cudaGetLastError();
-    const int grid = std::max(1, std::min(num_sms, max_units));
+    const int grid = std::max(1, std::min(g.max_ctas > 0 ? std::min(num_sms, g.max_ctas) : num_sms, max_units));
     cudaError_t e = sw ? launch_one<EPI_SWIGLU>(grid, ma, msh, mb, mb2, maf, mshf, p, stream)
                        : launch_one<EPI_PLAIN>(grid, ma, msh, mb, mb2, maf, mshf, p, stream);
     count_launches(1);

@@ -69,6 +69,7 @@ enum Epi : int { EPI_SWIGLU = 0, EPI_PLAIN = 1 };
 struct Params {
     int G, shared_group;
     int g_end;           // units cover the row tiles of groups [0, g_end)
+    int* sched;          // [2] device: next-unit counter and finished-CTA count, or nullptr (static order)
     const int32_t* offsets;
     const int32_t* tiles;
     int rows;            // single-group row count (offsets == nullptr)
@@ -168,11 +169,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             s_tiles[i] = __ldg(p.tiles + i);
             s_off[i] = __ldg(p.offsets + i);
         }
-    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kStages);
-    const uint32_t tfull0 = smem_u32(bars + 2 * kStages), tempty0 = smem_u32(bars + 2 * kStages + 2);
-    const uint32_t drain = smem_u32(bars + 2 * kStages + 4);
-    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kStages + 5);
+    // barrier block (256 bytes): stage full/empty [kMaxStages each], TMEM
+    // full/empty [2 each], drain, unit-ring full/empty [4 each], then the
+    // TMEM address, the abort flag and the 4-slot unit ring
+    const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
+    const uint32_t tfull0 = smem_u32(bars + 2 * kMaxStages), tempty0 = smem_u32(bars + 2 * kMaxStages + 2);
+    const uint32_t drain = smem_u32(bars + 2 * kMaxStages + 4);
+    const uint32_t ufull0 = smem_u32(bars + 2 * kMaxStages + 5), uempty0 = smem_u32(bars + 2 * kMaxStages + 9);
+    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kMaxStages + 13);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+    volatile int* s_units = (volatile int*)(tmem_slot + 2);
+    static_assert((2 * kMaxStages + 13) * 8 + 6 * 4 <= 256, "barrier block overflows");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -185,6 +192,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(tempty0 + 8 * b, 4);
         }
         mbar_init(drain, 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(ufull0 + 8 * i, 1);
+            mbar_init(uempty0 + 8 * i, 1 + 4);  // the MMA issuer and the 4 epilogue warps
+        }
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -211,7 +222,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, armed = 0, armed_parity = 0;
             const uint32_t b_bytes = (EPI == EPI_SWIGLU) ? 2u * 128 * BK * 2 : (uint32_t)p.BN * BK * 2;
             bool ok = true;
-            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            // units come from the launch-wide counter (CTAs that start late
+            // take fewer units) or in the static round-robin order; each is
+            // published to the MMA issuer and the epilogue through the unit
+            // ring.  The counter is drawn one unit ahead to hide its latency.
+            int next_u = p.sched ? atomicAdd(p.sched, 1) : blockIdx.x;
+            for (int i = 0; ok; ++i) {
+                int u = next_u;
+                if (u >= total_units) u = -1;
+                if (u >= 0) next_u = p.sched ? atomicAdd(p.sched, 1) : blockIdx.x + (i + 1) * gridDim.x;
+                if (!mbar_wait(uempty0 + 8 * (i & 3), ((i >> 2) & 1) ^ 1, lim, abort_flag)) {
+                    record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 5, blockIdx.x, i);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                s_units[i & 3] = u;
+                mbar_arrive(ufull0 + 8 * (i & 3));
+                if (u < 0) break;
                 const Unit un = decode_unit(p, u, total_tiles, s_tiles, s_off);
                 const bool sh = un.g == p.shared_group;
                 const CUtensorMap* ta = sh ? &tm_a_sh : &tm_a;
@@ -269,7 +297,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0, acc_phase = 0;
             const uint32_t idesc = p.in_f16 ? idesc_f16(BM, p.BN) : idesc_bf16(BM, p.BN);
             bool ok = true;
-            for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            for (int i = 0; ok; ++i) {
+                if (!mbar_wait(ufull0 + 8 * (i & 3), (i >> 2) & 1, lim, abort_flag)) {
+                    record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 6, blockIdx.x, i);
+                    *abort_flag = 1;
+                    break;
+                }
+                const int u = s_units[i & 3];
+                mbar_arrive(uempty0 + 8 * (i & 3));
+                if (u < 0) break;
                 if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, lim, abort_flag)) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 2, blockIdx.x, u);
                     *abort_flag = 1;
@@ -321,7 +357,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = sub * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
+        for (int i = 0;; ++i) {
+            int u = -1, got = 1;
+            if (lane == 0) {
+                got = mbar_wait(ufull0 + 8 * (i & 3), (i >> 2) & 1, lim, abort_flag);
+                if (got) {
+                    u = s_units[i & 3];
+                    mbar_arrive(uempty0 + 8 * (i & 3));
+                } else {
+                    record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 7, blockIdx.x, i);
+                    *abort_flag = 1;
+                }
+            }
+            got = __shfl_sync(0xffffffffu, got, 0);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            if (!got || u < 0) break;
             const Unit un = decode_unit(p, u, total_tiles, s_tiles, s_off);
             int ok = 1;
             if (lane == 0) {
@@ -423,6 +473,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(2 * kAccCols)
                      : "memory");
     }
+    if (p.sched && threadIdx.x == 0) {
+        // the last CTA to finish (every CTA's counter draws are done) rewinds
+        // the counters for the next launch on the stream
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1) == (int)gridDim.x - 1) {
+            atomicExch(p.sched, 0);
+            atomicExch(p.sched + 1, 0);
+        }
+    }
 }
 
 // ------------------------------------------------------------------- host
@@ -512,6 +571,7 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     Params p = {};
     p.G = g.offsets ? g.G : 1;
     p.g_end = (g.offsets && g.g_end > 0 && g.g_end < g.G) ? g.g_end : p.G;
+    p.sched = g.sched;
     p.shared_group = g.shared_group;
     p.offsets = g.offsets;
     p.tiles = g.tiles;
@@ -564,7 +624,7 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     }
     const int max_units = g.max_tiles * p.NB * p.KS;
     if (max_units <= 0) return cudaGetLastError();
-    const int grid = std::max(1, std::min(num_sms, max_units));
+    const int grid = std::max(1, std::min(g.max_ctas > 0 ? std::min(num_sms, g.max_ctas) : num_sms, max_units));
     cudaError_t e;
     if (sw) e = launch_one<EPI_SWIGLU, false>(grid, ma, msh, mb, mb2, maf, mshf, p, stream);
     else if (pair) e = launch_one<EPI_PLAIN, true>(grid, ma, msh, mb, mb2, maf, mshf, p, stream);

@@ -32,6 +32,8 @@ struct GroupedGemm {
     const int32_t* tiles;        // [G+1] device prefix of ceil(rows/128) (nullptr with offsets)
     const int32_t* tiles2;       // [G+1] device prefix of ceil(rows/256), or nullptr
     int g_end;                   // grouped tensor-core kernel only: work on groups [0, g_end) (0: all G)
+    int max_ctas;                // tensor-core kernels: at most this many CTAs (0: one per SM)
+    int* sched;                  // tensor-core kernels: [2] zeroed device ints for dynamic unit order, or nullptr
     int max_tiles2;              // host bound on the total number of 256-row tiles
     int prefer_pairs;            // 1: run on CTA pairs (M=256) when a kernel for it exists
     int rows;                    // single-group row count
