@@ -50,6 +50,11 @@ template <> __device__ __forceinline__ f16 from_f32<f16>(float v) { return __flo
 __device__ __forceinline__ uint8_t f32_to_e4m3(float v) {
     return (uint8_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
 }
+// Two values to two E4M3 codes (round to nearest even, saturating): a in
+// the low byte, b in the high byte.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float a, float b) {
+    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
 __device__ __forceinline__ float e4m3_to_f32(uint8_t q) {
     __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)q, __NV_E4M3);
     return __half2float(__half(hr));

@@ -283,13 +283,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int sub = warp & 3;      // TMEM lane quarter
         const int half = ew >> 2;      // which half of the columns
         const int row = sub * 32 + lane;
-        uint32_t chunk = 0, nunit = 0;
+        uint32_t chunk = 0;
         bool ok = true;
-        for (int i = 0; ok; ++i, ++nunit) {
-            int u = -1, got = 1;
+        for (int i = 0; ok; ++i) {
+            int u = -1;  // -1: no more units (or a wait that ran out)
             if (lane == 0) {
-                got = mbar_wait(ufull0 + 8 * (i & 3), (i >> 2) & 1, lim, abort_flag);
-                if (got) {
+                if (mbar_wait(ufull0 + 8 * (i & 3), (i >> 2) & 1, lim, abort_flag)) {
                     u = s_units[i & 3];
                     mbar_arrive(uempty0 + 8 * (i & 3));
                 } else {
@@ -297,10 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *abort_flag = 1;
                 }
             }
-            got = __shfl_sync(0xffffffffu, got, 0);
             u = __shfl_sync(0xffffffffu, u, 0);
-            if (!got || u < 0) break;
-            const int unit_par = nunit & 1;
+            if (u < 0) break;
+            const int unit_par = i & 1;
             const Unit un = decode_unit(p, u);
             const bool sh = un.g == p.shared_group;
             const int m = un.m0 + row;
@@ -376,9 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (EPI == EPI_SWIGLU) {
                 float amax = 0.0f;
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    acc[i] = swiglu(acc[i], acc[64 + i]);
-                    amax = fmaxf(amax, fabsf(acc[i]));
+                for (int c = 0; c < 64; ++c) {
+                    acc[c] = swiglu(acc[c], acc[64 + c]);
+                    amax = fmaxf(amax, fabsf(acc[c]));
                 }
                 // the two column halves of a row meet in shared memory; an
                 // mbarrier (bounded wait) rather than a named barrier, so an
@@ -387,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm[half * 128 + row] = amax;
                 const uint32_t xb = xbar0 + 8 * (unit_par * 4 + sub);
                 mbar_arrive(xb);
-                if (!mbar_wait(xb, (nunit >> 1) & 1u, lim, abort_flag)) {
+                if (!mbar_wait(xb, (i >> 1) & 1u, lim, abort_flag)) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 14, blockIdx.x, u);
                     *abort_flag = 1;
                     break;
@@ -405,11 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t w4[4];
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
-                            const int i = 16 * v + 4 * j;
-                            w4[j] = (uint32_t)f32_to_e4m3(__fmul_rn(acc[i], inv)) |
-                                    ((uint32_t)f32_to_e4m3(__fmul_rn(acc[i + 1], inv)) << 8) |
-                                    ((uint32_t)f32_to_e4m3(__fmul_rn(acc[i + 2], inv)) << 16) |
-                                    ((uint32_t)f32_to_e4m3(__fmul_rn(acc[i + 3], inv)) << 24);
+                            const int c = 16 * v + 4 * j;
+                            w4[j] = (uint32_t)f32x2_to_e4m3x2(__fmul_rn(acc[c], inv), __fmul_rn(acc[c + 1], inv)) |
+                                    ((uint32_t)f32x2_to_e4m3x2(__fmul_rn(acc[c + 2], inv), __fmul_rn(acc[c + 3], inv))
+                                     << 16);
                         }
                         *(uint4*)(o + 16 * v) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                     }
