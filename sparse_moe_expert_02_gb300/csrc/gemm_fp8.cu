@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nblocks = p.N / 128;
             float acc[128];
 #pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int c = 0; c < 128; ++c) acc[c] = 0.0f;
             // weight scale rows for this unit: [g][block][KB]
             const float* wsc1;
             const float* wsc2;
