@@ -178,6 +178,29 @@ def test_forward_replays_from_a_cuda_graph(shape):
     layer.check()
 
 
+@pytest.mark.parametrize("shape,T", [(synth.SMALL_BF16, 300), (synth.SMALL_BF16, 1), (synth.SMALL_FP8, 300),
+                                     (synth.SMALL_FP8, 129)], ids=["bf16_300", "bf16_1", "fp8_300", "fp8_129"])
+def test_forward_equals_stage_pipeline(shape, T):
+    """moe_forward runs the shared expert as its own GEMMs on a second stream
+    and the routed GEMMs over the routed groups only; the stage entry points
+    run every group in one grouped launch.  Same arithmetic, same order:
+    the outputs agree bit for bit."""
+    shape = shape.with_tokens(T)
+    inp = _dev_inputs(shape, seed=13)
+    layer = MoELayer.from_shape(shape, inp)
+    x = inp["x"]
+    a = layer.forward(x).clone()
+    layer.init_ws()
+    layer.route(x)
+    layer.permute(x)
+    layer.gemm_gateup(x)
+    layer.gemm_down(T)
+    b = layer.unpermute(T)
+    torch.cuda.synchronize()
+    layer.check()
+    assert torch.equal(a, b)
+
+
 # ------------------------------------------------------------- stage tests
 
 @pytest.mark.parametrize("T,E,k", [(300, 16, 2), (1000, 512, 10), (37, 1000, 32), (5, 7, 7)])
