@@ -261,7 +261,9 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
 // ---------------------------------------------------------------- gather
 
 // xp[p] = x[src_tok[p]] for p < rows; one warp per row, 16-byte vectors when
-// the row size allows, else 4-byte words.
+// the row size allows, else 4-byte words.  Each x row is read about top_k
+// times, so x should stay in L2 while xp (top_k times larger) streams out:
+// the stores carry the evict-first hint (st.global.cs).
 template <typename V>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const V* __restrict__ x, int64_t row_vecs,
                                                           const int32_t* __restrict__ src_tok, int rows,
@@ -277,9 +279,9 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const V* __restrict__ 
 #pragma unroll
             for (int u = 0; u < 8; ++u) t[u] = __ldg(src + i + 32 * u);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) dst[i + 32 * u] = t[u];
+            for (int u = 0; u < 8; ++u) __stcs(dst + i + 32 * u, t[u]);
         }
-        for (; i < row_vecs; i += 32) dst[i] = __ldg(src + i);
+        for (; i < row_vecs; i += 32) __stcs(dst + i, __ldg(src + i));
     }
 }
 
