@@ -351,6 +351,11 @@ moe_status moe_route(const moe_plan* p, const moe_weights* w, const void* x, int
 }
 
 namespace {
+// Permuted copy of x: from T >= 1024 tokens one warp per token reads its row
+// once and writes its top_k copies (x leaves DRAM once); below that there
+// are too few tokens to fill the GPU and one warp per output row gathers.
+bool scatter_by_token(int32_t T) { return T >= 1024; }
+
 // quant_x: the FP8 layer quantises x into xq here (false when the caller
 // already did).
 moe_status permute_impl(const moe_plan* p, const void* x, int32_t T, Ws& W, cudaStream_t s, bool quant_x) {
@@ -364,14 +369,22 @@ moe_status permute_impl(const moe_plan* p, const void* x, int32_t T, Ws& W, cuda
     if (c.dtype == MOE_FP8_E4M3_B128) {
         if (quant_x)
             MOE_CUDA(moe::launch_quant_rows(x, moe::kBF16, T, c.D, W.at<uint8_t>(W.L.xq), W.at<float>(W.L.xq_scale), s));
-        MOE_CUDA(moe::launch_gather_rows(W.at<uint8_t>(W.L.xq), 1, c.D, W.at<int32_t>(W.L.src_tok), TK,
-                                         W.at<uint8_t>(W.L.xp), s));
+        if (scatter_by_token(T))
+            MOE_CUDA(moe::launch_scatter_rows(W.at<uint8_t>(W.L.xq), c.D, W.at<int32_t>(W.L.inv), T, c.top_k,
+                                              W.at<uint8_t>(W.L.xp), s));
+        else
+            MOE_CUDA(moe::launch_gather_rows(W.at<uint8_t>(W.L.xq), 1, c.D, W.at<int32_t>(W.L.src_tok), TK,
+                                             W.at<uint8_t>(W.L.xp), s));
         MOE_CUDA(moe::launch_gather_rows(W.at<float>(W.L.xq_scale), 4, (int64_t)(c.D / 128) * 4,
                                          W.at<int32_t>(W.L.src_tok), TK, W.at<float>(W.L.xp_scale), s));
     } else {
         const int eb = act_bytes(c.dtype);
-        MOE_CUDA(moe::launch_gather_rows(x, eb, (int64_t)c.D * eb, W.at<int32_t>(W.L.src_tok), TK,
-                                         W.at<char>(W.L.xp), s));
+        if (scatter_by_token(T))
+            MOE_CUDA(moe::launch_scatter_rows(x, (int64_t)c.D * eb, W.at<int32_t>(W.L.inv), T, c.top_k,
+                                              W.at<char>(W.L.xp), s));
+        else
+            MOE_CUDA(moe::launch_gather_rows(x, eb, (int64_t)c.D * eb, W.at<int32_t>(W.L.src_tok), TK,
+                                             W.at<char>(W.L.xp), s));
     }
     return MOE_OK;
 }

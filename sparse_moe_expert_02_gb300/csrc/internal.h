@@ -90,6 +90,8 @@ cudaError_t launch_pack_words(const int32_t* blob, int64_t TK, int32_t* words, c
 cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_t* hist, int32_t* counts,
                                  int32_t* offsets, int32_t* tiles, int32_t* tiles2, int32_t* inv, int32_t* src_tok,
                                  uint32_t* err, cudaStream_t stream);
+cudaError_t launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t* inv, int T, int k, void* xp,
+                                cudaStream_t stream);
 cudaError_t launch_gather_rows(const void* x, int elem_bytes, int64_t row_bytes, const int32_t* src_tok,
                                int rows, void* xp, cudaStream_t stream);
 cudaError_t launch_quant_rows(const void* x, int x_elem, int rows, int cols, uint8_t* q, float* s,

@@ -146,6 +146,8 @@ __global__ void __launch_bounds__(32) perm_rank_kernel(const int32_t* __restrict
         if (e >= 0) {
             inv[a] = pos;
             src_tok[pos] = (int32_t)(a / k);
+        } else if (a < TK) {
+            inv[a] = -1;  // a dropped pair (its expert id was out of range)
         }
         if (a0 + s + 32 >= TK) break;
     }
@@ -228,6 +230,8 @@ __global__ void __launch_bounds__(1024) perm_index_small_kernel(const int32_t* _
         if (e >= 0) {
             inv[a] = pos;
             src_tok[pos] = a / k;
+        } else if (a < a1) {
+            inv[a] = -1;  // a dropped pair (its expert id was out of range)
         }
     }
 }
@@ -283,6 +287,57 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const V* __restrict__ 
         }
         for (; i < row_vecs; i += 32) __stcs(dst + i, __ldg(src + i));
     }
+}
+
+// xp[inv[t*k + j]] = x[t] for every token t and slot j: one warp per token
+// reads the row once (8 vectors per lane at a time) and writes it to its k
+// rows of the grouped layout, with the evict-first hint.  Each x row is
+// read from DRAM once, where a gather by output row reads it k times
+// through an L2 that the k-times larger output keeps flushing.  Dropped
+// pairs (inv < 0) are skipped.
+template <typename V>
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const V* __restrict__ x, int64_t row_vecs,
+                                                           const int32_t* __restrict__ inv, int T, int k,
+                                                           int64_t rows_out, V* __restrict__ xp) {
+    const int lane = threadIdx.x & 31;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
+        const int my = lane < k ? __ldg(inv + (int64_t)t * k + lane) : -1;
+        const V* src = x + (int64_t)t * row_vecs;
+        for (int64_t i0 = 0; i0 < row_vecs; i0 += 32 * 8) {
+            V v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t i = i0 + lane + 32 * u;
+                if (i < row_vecs) v[u] = __ldg(src + i);
+            }
+            for (int j = 0; j < k; ++j) {
+                const int r = __shfl_sync(0xffffffffu, my, j);
+                if (r < 0 || r >= rows_out) continue;
+                V* dst = xp + (int64_t)r * row_vecs;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int64_t i = i0 + lane + 32 * u;
+                    if (i < row_vecs) __stcs(dst + i, v[u]);
+                }
+            }
+        }
+    }
+}
+
+cudaError_t launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t* inv, int T, int k, void* xp,
+                                cudaStream_t stream) {
+    if (T <= 0) return cudaGetLastError();
+    const int blocks = (int)std::min<int64_t>(cdiv(T, 8), 148 * 16);
+    const int64_t rows_out = (int64_t)T * k;
+    if (row_bytes % 16 == 0)
+        scatter_rows_kernel<int4><<<blocks, 256, 0, stream>>>((const int4*)x, row_bytes / 16, inv, T, k, rows_out,
+                                                             (int4*)xp);
+    else
+        scatter_rows_kernel<int32_t><<<blocks, 256, 0, stream>>>((const int32_t*)x, row_bytes / 4, inv, T, k,
+                                                                rows_out, (int32_t*)xp);
+    count_launches(1);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gather_rows(const void* x, int elem_bytes, int64_t row_bytes, const int32_t* src_tok, int rows,
