@@ -357,31 +357,62 @@ cudaError_t launch_gather_rows(const void* x, int elem_bytes, int64_t row_bytes,
 // ------------------------------------------------------------- quantisers
 
 // Per row, per 128-column group: s = amax / 448 (1 if the group is all
-// zero), code = E4M3_rne_satfinite(fp32(v * fp32(448 / amax))).  One warp
-// per group, four columns per lane.
+// zero), code = E4M3_rne_satfinite(fp32(v * fp32(448 / amax))).  A half-warp
+// per group (8 bf16 = one 16-byte load per lane, 8 codes = one 8-byte store),
+// so a warp quantises two groups per step.
+__device__ __forceinline__ void load8f(const bf16* p, float* v) {
+    const uint4 raw = __ldg((const uint4*)p);
+    const __nv_bfloat162* h = (const __nv_bfloat162*)&raw;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void load8f(const float* p, float* v) {
+    const float4 a = __ldg((const float4*)p), b = __ldg((const float4*)p + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const T* __restrict__ x, int rows, int cols,
                                                          uint8_t* __restrict__ q, float* __restrict__ s) {
-    const int lane = threadIdx.x & 31;
+    const int lane = threadIdx.x & 31, sub = lane & 15;
     const int gpr = cols / 128;
     const int64_t ngroups = (int64_t)rows * gpr;
-    const int64_t warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; g < ngroups; g += warps) {
-        const int64_t r = g / gpr, c0 = (g % gpr) * 128 + lane * 4;
-        const T* src = x + r * cols + c0;
-        float v[4];
+    const int64_t halves = ((int64_t)gridDim.x * blockDim.x) >> 4;
+    // every lane walks the same number of steps, so the shuffles below see
+    // the whole warp; groups past the end compute on zeros and store nothing
+    const int64_t steps = (ngroups + halves - 1) / halves;
+    int64_t g = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+    for (int64_t it = 0; it < steps; ++it, g += halves) {
+        const bool ok = g < ngroups;
+        const int64_t r = ok ? g / gpr : 0;
+        const int64_t c0 = ok ? (g - r * gpr) * 128 + sub * 8 : 0;
+        float v[8];
+        if (ok) load8f(x + r * cols + c0, v);
+        else {
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = to_f32(src[i]);
-        float amax = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+            for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+        }
+        float amax = 0.0f;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
         float sc = __fdiv_rn(amax, 448.0f), inv = __fdiv_rn(448.0f, amax);
         if (amax == 0.0f) { sc = 1.0f; inv = 1.0f; }
-        uint32_t packed = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) packed |= (uint32_t)f32_to_e4m3(__fmul_rn(v[i], inv)) << (8 * i);
-        *(uint32_t*)(q + r * cols + c0) = packed;
-        if (lane == 0) s[g] = sc;
+        if (ok) {
+            uint2 packed;
+            packed.x = (uint32_t)f32x2_to_e4m3x2(__fmul_rn(v[0], inv), __fmul_rn(v[1], inv)) |
+                       ((uint32_t)f32x2_to_e4m3x2(__fmul_rn(v[2], inv), __fmul_rn(v[3], inv)) << 16);
+            packed.y = (uint32_t)f32x2_to_e4m3x2(__fmul_rn(v[4], inv), __fmul_rn(v[5], inv)) |
+                       ((uint32_t)f32x2_to_e4m3x2(__fmul_rn(v[6], inv), __fmul_rn(v[7], inv)) << 16);
+            *(uint2*)(q + r * cols + c0) = packed;
+            if (sub == 0) s[g] = sc;
+        }
     }
 }
 
@@ -389,7 +420,7 @@ cudaError_t launch_quant_rows(const void* x, int x_elem, int rows, int cols, uin
                               cudaStream_t stream) {
     if (rows <= 0) return cudaGetLastError();
     int64_t groups = (int64_t)rows * (cols / 128);
-    int blocks = (int)std::min<int64_t>(cdiv(groups, 8), 148 * 32);
+    int blocks = (int)std::min<int64_t>(cdiv(groups, 16), 148 * 32);
     if (x_elem == kBF16)
         quant_rows_kernel<bf16><<<blocks, 256, 0, stream>>>((const bf16*)x, rows, cols, q, s);
     else
