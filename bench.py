@@ -120,6 +120,12 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def out_dtype(shape) -> str:
+    """Layer output: fp32 for the fp32 layer, bf16 (the activations' type) for
+    the bf16 and FP8 layers."""
+    return "f32" if shape.dtype == "f32" else "bf16"
+
+
 def algorithmic(shape, counts: np.ndarray):
     """Bytes and flops the method itself must move and compute (no padding,
     no intermediate round trips): touched routed experts + shared expert +
@@ -127,10 +133,11 @@ def algorithmic(shape, counts: np.ndarray):
     D, E, I, k, T = shape.D, shape.E, shape.I, shape.top_k, shape.T
     bw = {"f32": 4, "bf16": 2, "fp8": 1}[shape.dtype]
     bx = 4 if shape.dtype == "f32" else 2
+    bo = 4 if out_dtype(shape) == "f32" else 2
     touched = int((counts[:E] > 0).sum())
     scale_bytes = (3 * (I // 128) * (D // 128) * 4) if shape.dtype == "fp8" else 0
     per_expert = 3 * D * I * bw + scale_bytes
-    layer_bytes = (touched + 1) * per_expert + E * D * bx + T * D * bx + T * D * 4 + 8 * T * k
+    layer_bytes = (touched + 1) * per_expert + E * D * bx + T * D * bx + T * D * bo + 8 * T * k
     flops = T * (2 * D * E + (k + 1) * 6 * D * I)
     gu_bytes = (touched + 1) * (2 * I * D * bw + 2 * scale_bytes // 3) + (T * k + T) * D * bw + (T * k + T) * I * bw
     dn_bytes = (touched + 1) * (D * I * bw + scale_bytes // 3) + (T * k + T) * I * bw + (T * k + T) * D * 2
@@ -162,7 +169,7 @@ def run_ours(args, shape, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     inp = synth.make_inputs(shape, seed=args.seed, device=dev)
-    layer = MoELayer.from_shape(shape, inp, device=local, flags=args.flags)
+    layer = MoELayer.from_shape(shape, inp, device=local, flags=args.flags, out_dtype=out_dtype(shape))
     x = inp["x"]
     T = shape.T
     out = layer.new_out(T)
@@ -285,6 +292,7 @@ def run_ours(args, shape, world, rank, local):
         "data": "synthetic (seeded; random-init weights of the layer's shape)",
         "config": {"workload": shape.name, "T": T, "D": shape.D, "E": shape.E, "I": shape.I,
                    "top_k": shape.top_k, "shared_experts": 1, "router_bias_zipf_s": shape.zipf_s,
+                   "out_dtype": out_dtype(shape),
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (expert weights stream from HBM every step)",
                    "touched_experts": alg["touched_experts"]},

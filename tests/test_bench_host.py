@@ -54,7 +54,9 @@ def test_algorithmic_accounting():
     D, I, E, T, k = shape.D, shape.I, shape.E, shape.T, shape.top_k
     per_expert = 3 * D * I * 2
     assert a["touched_experts"] == 475
-    assert a["layer_bytes"] == 476 * per_expert + E * D * 2 + T * D * 2 + T * D * 4 + 8 * T * k
+    # bf16 x in, bf16 out (the bf16 layer's output), 8 bytes of routing per slot
+    assert bench.out_dtype(shape) == "bf16" and bench.out_dtype(synth.TINY_F32) == "f32"
+    assert a["layer_bytes"] == 476 * per_expert + E * D * 2 + T * D * 2 + T * D * 2 + 8 * T * k
     assert a["flops"] == T * (2 * D * E + (k + 1) * 6 * D * I)
     assert a["gemm_gateup_bytes"] > 476 * 2 * I * D * 2
 
