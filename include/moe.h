@@ -274,6 +274,13 @@ MOE_API moe_status moe_pack_routing_words(const moe_plan* plan, int32_t T, const
 MOE_API moe_status moe_convert_down_weights(const moe_plan* plan, const void* w_down, void* w_down_f16, void* ws,
                                             size_t ws_bytes, void* stream);
 
+/* Where a pointer lives, as the device sees it: *kind = 0 host memory the
+ * device cannot address, 1 page-locked host memory mapped at the same address
+ * (a kernel may read or write it directly, e.g. moe_forward's `out`, so the
+ * result lands in host memory without a separate copy), 2 device memory,
+ * 3 managed memory.  Synchronous, enqueues nothing. */
+MOE_API moe_status moe_pointer_kind(const void* p, int32_t* kind);
+
 /* Synchronise `stream`, read the workspace error word and return the first
  * device-side error recorded since the last clear (MOE_OK if none). */
 MOE_API moe_status moe_check(const moe_plan* plan, const void* ws, void* stream);

@@ -37,7 +37,7 @@ SYMBOLS = (
     "moe_workspace_init", "moe_quantize_weights", "moe_forward", "moe_route", "moe_topk", "moe_permute",
     "moe_gemm_gateup", "moe_gemm_down", "moe_unpermute", "moe_check", "moe_selftest_wait_timeout",
     "moe_status_str", "moe_last_error_detail", "moe_build_info", "moe_launch_count",
-    "moe_permute_index_noalloc", "moe_pack_routing_words", "moe_convert_down_weights",
+    "moe_permute_index_noalloc", "moe_pack_routing_words", "moe_convert_down_weights", "moe_pointer_kind",
 )
 
 
@@ -104,6 +104,7 @@ def lib():
                 "moe_permute_index_noalloc": (st, [P, I32, I32, I32, P, P, P, P, P, P]),
                 "moe_pack_routing_words": (st, [P, I32, P, S, P, P]),
                 "moe_convert_down_weights": (st, [P, P, P, P, S, P]),
+                "moe_pointer_kind": (st, [P, ctypes.POINTER(ctypes.c_int32)]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -113,15 +114,20 @@ def lib():
     return _lib
 
 
-def _ptr(t):
+def _ptr(t, host_mapped_ok: bool = False):
+    """Address of a contiguous device tensor; with host_mapped_ok also of a
+    page-locked host tensor that the device addresses at the same place
+    (moe_pointer_kind == host_mapped), which kernels then read or write
+    directly."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
-    if not t.is_cuda:
-        raise ValueError("libmoe takes device tensors")
     if not t.is_contiguous():
         raise ValueError("libmoe takes contiguous tensors")
+    if not t.is_cuda:
+        if not (host_mapped_ok and t.is_pinned() and moe_pointer_kind(t) == "host_mapped"):
+            raise ValueError("libmoe takes device tensors (or, for out, mapped page-locked host tensors)")
     return t.data_ptr()
 
 
@@ -174,6 +180,16 @@ def moe_quantize_weights(plan, w, q, s, stream=None):
         "moe_quantize_weights")
 
 
+POINTER_KINDS = {0: "host", 1: "host_mapped", 2: "device", 3: "managed"}
+
+
+def moe_pointer_kind(t) -> str:
+    k = ctypes.c_int32(0)
+    p = t if isinstance(t, int) else t.data_ptr()
+    _ok(lib().moe_pointer_kind(p, ctypes.byref(k)), "moe_pointer_kind")
+    return POINTER_KINDS.get(k.value, "host")
+
+
 def moe_convert_down_weights(plan, w_down, w_down_f16, ws, stream=None):
     _ok(lib().moe_convert_down_weights(plan, _ptr(w_down), _ptr(w_down_f16), _ptr(ws), _wsb(ws), _stream(stream)),
         "moe_convert_down_weights")
@@ -189,7 +205,8 @@ def _wsb(ws):
 
 
 def moe_forward(plan, weights: moe_weights, x, T, out, blob_out, logits_out, ws, stream=None):
-    _ok(lib().moe_forward(plan, ctypes.byref(weights), _ptr(x), T, _ptr(out), _ptr(blob_out), _ptr(logits_out),
+    _ok(lib().moe_forward(plan, ctypes.byref(weights), _ptr(x), T, _ptr(out, host_mapped_ok=True), _ptr(blob_out),
+                          _ptr(logits_out),
                           _ptr(ws), _wsb(ws), _stream(stream)), "moe_forward")
 
 

@@ -615,6 +615,23 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
     return MOE_OK;
 }
 
+moe_status moe_pointer_kind(const void* ptr, int32_t* kind) {
+    if (!kind) return arg_fail(MOE_ERR_INVALID_ARG, "kind is NULL");
+    *kind = 0;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+        cudaGetLastError();  // unregistered host memory on older drivers
+        return MOE_OK;
+    }
+    switch (a.type) {
+        case cudaMemoryTypeDevice: *kind = 2; break;
+        case cudaMemoryTypeManaged: *kind = 3; break;
+        case cudaMemoryTypeHost: *kind = (a.devicePointer == ptr) ? 1 : 0; break;
+        default: *kind = 0; break;
+    }
+    return MOE_OK;
+}
+
 moe_status moe_convert_down_weights(const moe_plan* p, const void* w_down, void* w_down_f16, void* ws,
                                    size_t ws_bytes, void* stream) {
     if (!p) return arg_fail(MOE_ERR_INVALID_ARG, "plan is NULL");

@@ -201,6 +201,27 @@ def test_forward_equals_stage_pipeline(shape, T):
     assert torch.equal(a, b)
 
 
+def test_forward_into_mapped_host_memory():
+    """out may be page-locked host memory that the device addresses directly:
+    the unpermute then writes the result there, bit-identical to a device
+    out copied back."""
+    shape = synth.SMALL_BF16
+    inp = _dev_inputs(shape, seed=14)
+    layer = MoELayer.from_shape(shape, inp, out_dtype="bf16")
+    ref = layer.forward(inp["x"]).cpu()
+    out_h = torch.empty((shape.T, shape.D), dtype=torch.bfloat16).pin_memory()
+    assert L.moe_pointer_kind(layer.ws) == "device"
+    if L.moe_pointer_kind(out_h) != "host_mapped":
+        pytest.skip("page-locked host memory is not mapped at the same address on this system")
+    out_h.zero_()
+    layer.forward(inp["x"], out_h)
+    torch.cuda.synchronize()
+    layer.check()
+    assert torch.equal(out_h, ref)
+    with pytest.raises(ValueError):  # ordinary (pageable) host memory is refused before any launch
+        layer.forward(inp["x"], torch.empty((shape.T, shape.D), dtype=torch.bfloat16))
+
+
 # ------------------------------------------------------------- stage tests
 
 @pytest.mark.parametrize("T,E,k", [(300, 16, 2), (1000, 512, 10), (37, 1000, 32), (5, 7, 7)])
