@@ -163,7 +163,8 @@ typedef struct moe_ws_layout {
 } moe_ws_layout;
 
 /* Validate a configuration and build a host-side plan for `device`.
- * Supported: D, I multiples of 128 (64 for MOE_F32), E <= 1024,
+ * Supported: D, I multiples of 128 (64 for MOE_F32; D a multiple of 256 for
+ * MOE_FP8_E4M3_B128), E <= 1024,
  * 1 <= top_k <= min(E, 32), 1 <= T_max <= 2^20, T_max*(top_k+1) < 2^31.
  * The plan owns no device memory; it holds one CUDA stream and two events
  * on `device` (see moe_forward).  *out is NULL on error. */

@@ -226,6 +226,8 @@ moe_status moe_plan_create(const moe_config* cfg, int device, moe_plan** out) {
     const int q = (c.dtype == MOE_F32) ? 64 : 128;
     if (c.D < q || c.D % q || c.I < q || c.I % q) return arg_fail(MOE_ERR_UNSUPPORTED, "D and I must be multiples of 128 (64 for fp32)");
     if (c.D > 65536 || c.I > 65536) return arg_fail(MOE_ERR_UNSUPPORTED, "D or I above 65536");
+    if (c.dtype == MOE_FP8_E4M3_B128 && c.D % 256)  // the FP8 down GEMM's units are 256 output features wide
+        return arg_fail(MOE_ERR_UNSUPPORTED, "the FP8 layer needs D a multiple of 256");
     if (c.spin_limit_ns < 0) return arg_fail(MOE_ERR_INVALID_ARG, "spin_limit_ns < 0");
     int ndev = 0;
     if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev)

@@ -53,6 +53,7 @@ def test_status_strings_and_build_info():
     (dict(top_k=33, E=64), L.MOE_ERR_UNSUPPORTED),
     (dict(top_k=17, E=16), L.MOE_ERR_UNSUPPORTED),
     (dict(D=200), L.MOE_ERR_UNSUPPORTED),
+    (dict(D=128, dtype=2), L.MOE_ERR_UNSUPPORTED),  # FP8: the down GEMM's units are 256 features wide
     (dict(I=100), L.MOE_ERR_UNSUPPORTED),
     (dict(T_max=0), L.MOE_ERR_UNSUPPORTED),
     (dict(T_max=(1 << 20) + 1), L.MOE_ERR_UNSUPPORTED),

@@ -108,6 +108,18 @@ def test_small_bf16_layer(flags, T):
     _layer_parity(shape, _dev_inputs(shape, seed=4), flags=flags)
 
 
+@pytest.mark.parametrize("shape", [
+    synth.LayerShape("edge_bf16_one_expert_T5_D128_E1_I128_k1", 5, 128, 1, 128, 1, "bf16"),
+    synth.LayerShape("edge_bf16_E1024_k32_T70_D256_I128", 70, 256, 1024, 128, 32, "bf16", 1.0),
+    synth.LayerShape("edge_fp8_T3_D256_E2_I128_k2", 3, 256, 2, 128, 2, "fp8"),
+    synth.LayerShape("edge_f32_T1_D64_E1_I64_k1", 1, 64, 1, 64, 1, "f32"),
+], ids=["bf16_E1_k1", "bf16_E1024_k32", "fp8_E2", "f32_E1_T1"])
+def test_edge_shapes(shape):
+    """Smallest dimensions the plan accepts, one expert, and the largest E
+    and top_k: routing bit-exact, output within tolerance."""
+    _layer_parity(shape, _dev_inputs(shape, seed=15))
+
+
 def test_small_bf16_bf16_output():
     shape = synth.SMALL_BF16
     inp = _dev_inputs(shape, seed=5)
