@@ -6,8 +6,9 @@
 // "Fusing Three Collectives Into Two": indices and weights, both [T, k],
 // travel as one 32-bit integer blob.
 //
-// One warp per token.  Each lane keeps E/32 logits in registers; k rounds of
-// a warp-wide argmax pick the experts.  Order: larger logit first, the lower
+// One warp per token.  Each lane keeps E/32 logits in registers and its four
+// best in order; k rounds of a warp-wide argmax over the lanes' heads pick
+// the experts.  Order: larger logit first, the lower
 // expert index on equal logits -- the same total order in every lane and in
 // the cross-lane reduction, so the choice is deterministic.  Weights are the
 // softmax over the chosen logits (equal to the renormalised full softmax).
@@ -77,9 +78,10 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
         for (int j = 0; j < J; ++j)
             if (!isfinite(v[j])) v[j] = -INFINITY;
     }
-    // Each lane sorts its logits once: larger first, lower expert index first
-    // among equals (the lane's experts are lane, lane+32, ...).  Key 0 marks
-    // an empty slot: every real logit (even -inf) has a larger key.
+    // Each lane keeps its H best (key, expert) pairs in order -- larger logit
+    // first, the lower expert index among equals -- built by insertion over
+    // its J logits.  Key 0 marks an empty slot: every real logit (even -inf)
+    // has a larger key.
     uint32_t key[J];
     int id[J];
 #pragma unroll
@@ -88,40 +90,63 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
         key[j] = (e < E) ? order_key(v[j]) : 0u;
         id[j] = e;
     }
+    constexpr int H = J < 4 ? J : 4;
+    uint32_t hk[H];
+    int hi[H];
+    // the H best of this lane's pairs that come strictly after (ak, ai) in the
+    // order (all of them when `all`)
+    auto build = [&](bool all, uint32_t ak, int ai) {
 #pragma unroll
-    for (int size = 2; size <= J; size <<= 1)
+        for (int h = 0; h < H; ++h) {
+            hk[h] = 0u;
+            hi[h] = 0x7FFFFFFF;
+        }
 #pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1)
+        for (int j = 0; j < J; ++j) {
+            const uint32_t kj = key[j];
+            const int ij = id[j];
+            const bool after = all || kj < ak || (kj == ak && ij > ai);
+            if (after && (kj > hk[H - 1] || (kj == hk[H - 1] && ij < hi[H - 1]))) {
+                hk[H - 1] = kj;
+                hi[H - 1] = ij;
 #pragma unroll
-            for (int i = 0; i < J; ++i) {
-                const int l = i ^ stride;
-                if (l > i) {
-                    const bool first_up = (i & size) == 0;  // keep the better one at i
-                    const bool l_better = key[l] > key[i] || (key[l] == key[i] && id[l] < id[i]);
-                    if (l_better == first_up) {
-                        const uint32_t tk = key[i]; key[i] = key[l]; key[l] = tk;
-                        const int ti = id[i]; id[i] = id[l]; id[l] = ti;
+                for (int h = H - 1; h > 0; --h) {
+                    if (hk[h] > hk[h - 1] || (hk[h] == hk[h - 1] && hi[h] < hi[h - 1])) {
+                        const uint32_t tk = hk[h]; hk[h] = hk[h - 1]; hk[h - 1] = tk;
+                        const int ti = hi[h]; hi[h] = hi[h - 1]; hi[h - 1] = ti;
                     }
                 }
             }
+        }
+    };
+    build(true, 0u, 0);
     // k rounds: the largest head over the warp, the lowest index among the
-    // lanes holding it; that lane drops its head.
+    // lanes holding it; that lane drops its head (and, having used all H,
+    // rebuilds its list from the pairs after the one it gave up).
     float zsel = 0.0f;
     int isel = 0;
+    int used = 0;
     for (int r = 0; r < k; ++r) {
-        const uint32_t m = __reduce_max_sync(0xffffffffu, key[0]);
-        const uint32_t win = __reduce_min_sync(0xffffffffu, key[0] == m ? (uint32_t)id[0] : 0xFFFFFFFFu);
+        const uint32_t m = __reduce_max_sync(0xffffffffu, hk[0]);
+        const uint32_t win = __reduce_min_sync(0xffffffffu, hk[0] == m ? (uint32_t)hi[0] : 0xFFFFFFFFu);
         if (lane == r) {
             zsel = key_value(m);
             isel = (int)win;
         }
-        if (key[0] == m && (uint32_t)id[0] == win) {
+        if (hk[0] == m && (uint32_t)hi[0] == win) {
+            const uint32_t lk = hk[0];
+            const int li = hi[0];
 #pragma unroll
-            for (int j = 0; j + 1 < J; ++j) {
-                key[j] = key[j + 1];
-                id[j] = id[j + 1];
+            for (int h = 0; h + 1 < H; ++h) {
+                hk[h] = hk[h + 1];
+                hi[h] = hi[h + 1];
             }
-            key[J - 1] = 0u;
+            hk[H - 1] = 0u;
+            hi[H - 1] = 0x7FFFFFFF;
+            if (++used == H) {
+                build(false, lk, li);
+                used = 0;
+            }
         }
     }
     const float zmax = __shfl_sync(0xffffffffu, zsel, 0);
