@@ -112,44 +112,68 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ h
 
 // ------------------------------------------------------------------ rank
 
-__global__ void __launch_bounds__(32) perm_rank_kernel(const int32_t* __restrict__ idx, int64_t TK, int k, int E,
-                                                       const int32_t* __restrict__ hist,
-                                                       const int32_t* __restrict__ offsets,
-                                                       int32_t* __restrict__ inv, int32_t* __restrict__ src_tok) {
-    extern __shared__ int32_t cursor[];
-    const int lane = threadIdx.x;
+// One block of 8 warps per chunk: warp w owns the w-th eighth of the chunk's
+// pairs.  Each warp counts its pairs per expert, the block turns the counts
+// into per-warp cursors (chunk start from the scan, plus the counts of the
+// warps before), and each warp then ranks its pairs in order, 32 at a time,
+// ranking equal experts inside a step with __match_any_sync.
+constexpr int kRankWarps = 8;
+
+__global__ void __launch_bounds__(32 * kRankWarps) perm_rank_kernel(const int32_t* __restrict__ idx, int64_t TK,
+                                                                    int k, int E,
+                                                                    const int32_t* __restrict__ hist,
+                                                                    const int32_t* __restrict__ offsets,
+                                                                    int32_t* __restrict__ inv,
+                                                                    int32_t* __restrict__ src_tok) {
+    extern __shared__ int32_t cur[];  // [kRankWarps][E]: counts, then cursors
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunk = perm_chunk(TK);
-    const int64_t a0 = (int64_t)blockIdx.x * chunk;
-    // the chunk's expert ids, all loaded before the walk (chunk <= 32 * 32)
-    int ids[kPermChunk / 32];
+    const int per = chunk / kRankWarps;  // pairs per warp (16 or 128)
+    const int64_t a0 = (int64_t)blockIdx.x * chunk + (int64_t)warp * per;
+    constexpr int kSteps = kPermChunk / kRankWarps / 32;
+    int ids[kSteps];
 #pragma unroll
-    for (int s = 0; s < kPermChunk / 32; ++s) {
+    for (int s = 0; s < kSteps; ++s) {
         const int64_t a = a0 + 32 * s + lane;
-        ids[s] = (32 * s < chunk && a < TK) ? __ldg(idx + a) : -1;
+        int e = (32 * s + lane < per && a < TK) ? __ldg(idx + a) : -1;
+        if ((unsigned)e >= (unsigned)E) e = -1;  // out-of-range ids were reported by hist
+        ids[s] = e;
     }
-    for (int e = lane; e < E; e += 32) cursor[e] = __ldg(offsets + e) + __ldg(hist + (int64_t)blockIdx.x * E + e);
-    __syncwarp();
+    for (int i = threadIdx.x; i < kRankWarps * E; i += blockDim.x) cur[i] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int s = 0; s < kSteps; ++s)
+        if (ids[s] >= 0) atomicAdd(&cur[warp * E + ids[s]], 1);
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = __ldg(offsets + e) + __ldg(hist + (int64_t)blockIdx.x * E + e);
+#pragma unroll
+        for (int w = 0; w < kRankWarps; ++w) {
+            const int c = cur[w * E + e];
+            cur[w * E + e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    int32_t* cw = cur + warp * E;
     const unsigned lt = (1u << lane) - 1u;
 #pragma unroll
-    for (int si = 0; si < kPermChunk / 32; ++si) {
-        const int s = 32 * si;
-        if (s >= chunk) break;
-        const int64_t a = a0 + s + lane;
-        int e = ids[si];
-        if ((unsigned)e >= (unsigned)E) e = -1;  // out-of-range ids were reported by hist
+    for (int s = 0; s < kSteps; ++s) {
+        if (32 * s >= per) break;
+        const int64_t a = a0 + 32 * s + lane;
+        const int e = ids[s];
         const unsigned peers = __match_any_sync(0xffffffffu, e);
         int pos = 0;
-        if (e >= 0) pos = cursor[e] + __popc(peers & lt);
+        if (e >= 0) pos = cw[e] + __popc(peers & lt);
         __syncwarp();
-        if (e >= 0 && (peers >> lane) == 1u) cursor[e] += __popc(peers);  // highest lane of the group
+        if (e >= 0 && (peers >> lane) == 1u) cw[e] += __popc(peers);  // highest lane of the group
         __syncwarp();
         if (e >= 0) {
             inv[a] = pos;
             src_tok[pos] = (int32_t)(a / k);
-        } else if (a < TK) {
+        } else if (32 * s + lane < per && a < TK) {
             inv[a] = -1;  // a dropped pair (its expert id was out of range)
         }
-        if (a0 + s + 32 >= TK) break;
     }
 }
 
@@ -257,7 +281,14 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
     const int nch = (int)cdiv(TK, perm_chunk(TK));
     perm_hist_kernel<<<nch, 256, E * sizeof(int32_t), stream>>>(idx, TK, E, hist, err);
     perm_scan_kernel<<<1, 1024, 0, stream>>>(hist, nch, E, T, counts, offsets, tiles, tiles2, src_tok, TK);
-    perm_rank_kernel<<<nch, 32, E * sizeof(int32_t), stream>>>(idx, TK, k, E, hist, offsets, inv, src_tok);
+    static int rank_smem_set = 0;
+    const int rank_smem = kRankWarps * E * (int)sizeof(int32_t);
+    if (rank_smem > 48 * 1024 && rank_smem_set < rank_smem) {
+        cudaError_t e = cudaFuncSetAttribute(perm_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, rank_smem);
+        if (e != cudaSuccess) return e;
+        rank_smem_set = rank_smem;
+    }
+    perm_rank_kernel<<<nch, 32 * kRankWarps, rank_smem, stream>>>(idx, TK, k, E, hist, offsets, inv, src_tok);
     count_launches(3);
     return cudaGetLastError();
 }
