@@ -11,11 +11,16 @@
 // feature block minor, so the CTAs that run at the same time share a row tile
 // (A read once) and the row tiles of a group run back to back (its weight
 // block is reused from L2).  The row tiles come from the device-built prefix
-// of ceil(rows/128) per group; no host round trip.
+// of ceil(rows/128) per group (copied to shared memory); no host round trip.
+// A CTA takes its units either in the static round-robin order or, given a
+// counter, from a launch-wide atomic (so that CTAs which start late, behind a
+// kernel on another stream, take fewer); the producer draws them and hands
+// them to the other roles through a 4-slot ring in shared memory.
 //
 // Warp roles (192 threads, one CTA per SM):
-//   warp 0      TMA producer: A rows (16-row boxes, only the boxes that hold
-//               valid rows) and the B weight tile into a 4-stage ring;
+//   warp 0      TMA producer: A rows (one 128-row box for a full tile, else
+//               16-row boxes, only those that hold valid rows) and the B
+//               weight tile into a ring of 4-8 stages (as many as fit);
 //   warp 1      TMEM allocator and MMA issuer: tcgen05.mma kind::f16,
 //               M=128, N=BN, K=16, fp32 accumulation in TMEM;
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (two TMEM buffers,
