@@ -583,10 +583,14 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     p.rows = g.rows;
     p.BN = sw ? 256 : plain_bn(g.N);
     if (!sw && !g.offsets) {
-        // single group (router): narrow the feature block until the units
-        // cover the SMs (T=128 at E=512: 16 units of 32 experts, not 2 of 256)
+        // single group (router): narrow the feature block while twice the
+        // units (K slices included) still fit in one wave on the SMs (T=128 at
+        // E=512 with 8 K slices: 16 x 8 units of 32 experts; T=1024: 2 x 8
+        // units of 8 row tiles x 256 experts)
         const int row_tiles = (g.rows + BM - 1) / BM;
-        while (p.BN > 32 && g.N % (p.BN / 2) == 0 && (p.BN / 2) % 32 == 0 && row_tiles * (g.N / p.BN) < num_sms)
+        const int ks = (g.ksplit > 1 && (g.Kb / BK) % g.ksplit == 0) ? g.ksplit : 1;
+        while (p.BN > 32 && g.N % (p.BN / 2) == 0 && (p.BN / 2) % 32 == 0 &&
+               row_tiles * (g.N / p.BN) * ks * 2 <= num_sms)
             p.BN /= 2;
     }
     p.NB = sw ? g.N / 128 : g.N / p.BN;

@@ -203,10 +203,11 @@ cudaError_t launch_pack_words(const int32_t* blob, int64_t TK, int32_t* words, c
     return cudaGetLastError();
 }
 
-// K slices of the router GEMM: enough (up to 8) that the units of 32
-// experts x 128 tokens x K/S cover the SMs when T is small.
+// K slices of the router GEMM: up to 8, while twice the units of 256 experts
+// x 128 tokens x K/S still fit in one wave on the SMs (the GEMM then narrows
+// its expert block only if even that leaves SMs idle: decode-sized T).
 int router_splits(int T, int E, int D, int num_sms) {
-    const int units = (int)cdiv(T, 128) * std::max(1, E / 32);
+    const int units = (int)cdiv(T, 128) * std::max(1, E / 256);
     const int kblocks = D / 64;
     int S = 1;
     while (S < 8 && units * S * 2 <= num_sms && kblocks % (2 * S) == 0) S *= 2;
