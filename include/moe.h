@@ -104,6 +104,14 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2 } moe_
 #define MOE_FLAG_PAIR_CTA_OFF 0x2u /* bf16 expert GEMMs never on CTA pairs (the default) */
 #define MOE_FLAG_PAIR_CTA_ON 0x4u  /* bf16 expert GEMMs on CTA pairs (cta_group::2, 256-row tiles) */
 #define MOE_FLAG_DOWN_HILO 0x8u    /* bf16 layer: h as a bf16 hi/lo pair, bf16 W_down (no w_down_f16) */
+/* Tile pairs: the bf16 layer's tensor-core expert GEMMs run on 2-CTA
+ * clusters whose CTAs share one operand tile through TMA multicast (two
+ * 128-row tiles of an expert against one weight block, or a group's odd last
+ * tile against two weight blocks), so each SM reads fewer operand bytes from
+ * L2 per MMA; results are identical.  By default they are used when
+ * T * top_k >= 64 * E (at least 64 rows per expert on average: prefill). */
+#define MOE_FLAG_MCAST_ON 0x10u    /* tile pairs whenever the shape allows them */
+#define MOE_FLAG_MCAST_OFF 0x20u   /* never tile pairs */
 
 typedef struct moe_config {
     int32_t T_max;           /* largest token count a call may pass */

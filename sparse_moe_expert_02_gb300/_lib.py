@@ -28,6 +28,8 @@ MOE_FLAG_FORCE_SIMT = 0x1
 MOE_FLAG_PAIR_CTA_OFF = 0x2
 MOE_FLAG_PAIR_CTA_ON = 0x4
 MOE_FLAG_DOWN_HILO = 0x8
+MOE_FLAG_MCAST_ON = 0x10
+MOE_FLAG_MCAST_OFF = 0x20
 
 DTYPE_CODE = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8": MOE_FP8_E4M3_B128}
 

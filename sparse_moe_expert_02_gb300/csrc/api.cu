@@ -178,6 +178,16 @@ int prefer_pairs(const moe_plan* p, int T) {
     return (p->cfg.flags & MOE_FLAG_PAIR_CTA_ON) ? 1 : 0;
 }
 
+// Tile pairs (2-CTA clusters sharing operand tiles) pay where groups hold
+// several row tiles; at decode sizes the GEMMs stream weights from HBM and the
+// clusters only couple the CTAs' progress.
+int prefer_mcast(const moe_plan* p, int T) {
+    const uint32_t f = p->cfg.flags;
+    if (f & MOE_FLAG_MCAST_OFF) return 0;
+    if (f & MOE_FLAG_MCAST_ON) return 1;
+    return (int64_t)T * p->cfg.top_k >= 64 * (int64_t)p->cfg.E ? 1 : 0;
+}
+
 int grouped_max_tiles2(const moe_config& c, int T) {
     const int64_t R = (int64_t)T * (c.top_k + 1);
     return (int)(R / (2 * moe::kRowTile) + c.E + 2);
@@ -414,6 +424,7 @@ moe::GroupedGemm gateup_gemm(const moe_plan* p, const moe_weights* w, const void
     g.tiles2 = W.at<int32_t>(W.L.tiles2);
     g.max_tiles2 = grouped_max_tiles2(c, T);
     g.prefer_pairs = prefer_pairs(p, T);
+    g.mcast = prefer_mcast(p, T);
     g.N = c.I;
     g.Ka = g.Kb = c.D;
     g.out_pair = hilo(c);
@@ -450,6 +461,7 @@ moe::GroupedGemm down_gemm(const moe_plan* p, const moe_weights* w, int32_t T, W
     g.tiles2 = W.at<int32_t>(W.L.tiles2);
     g.max_tiles2 = grouped_max_tiles2(c, T);
     g.prefer_pairs = prefer_pairs(p, T);
+    g.mcast = prefer_mcast(p, T);
     g.N = c.D;
     g.Kb = c.I;
     g.Ka = hilo(c) ? 2 * c.I : c.I;  // the hi/lo pair walks W_down twice

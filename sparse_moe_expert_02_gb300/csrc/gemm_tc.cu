@@ -26,6 +26,16 @@
 //   warps 2..5  epilogue: tcgen05.ld of the accumulator (two TMEM buffers,
 //               so the epilogue of one unit overlaps the MMAs of the next),
 //               SwiGLU / bias / conversion, stores.
+// Tile pairs (prefill): the CTAs run as 2-CTA clusters whose two CTAs share
+// one operand tile through TMA multicast, so each SM pulls fewer operand
+// bytes from L2 per MMA.  A cluster unit is either two row tiles of one
+// group against one weight block (each CTA copies half of the 256-row B tile
+// into both CTAs: 16 KB of A + 16 KB of B per CTA and stage instead of
+// 16 + 32) or, for a group's odd last row tile, that tile against two weight
+// blocks (each CTA copies half of the A rows into both: 8 + 32).  Row tiles
+// stay 128 rows, so no padding is added.  Each CTA's stage is written by both
+// CTAs, so both MMA issuers' commits release it (commit multicast), and the
+// cluster synchronises before it exits.
 // Operands are K-major with the 128-byte swizzle on both sides (TMA writes
 // it, the UMMA descriptor reads it).  Every mbarrier wait is bounded by
 // spin_ns; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its
@@ -129,6 +139,47 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u, int total_ti
     return r;
 }
 
+// Tile pairs: cluster unit v, seen from the CTA of rank `rank`.  A group of
+// t row tiles has t * NB / 2 cluster units: first (t / 2) * NB "B-shared"
+// ones (row tiles 2q + rank against weight block nb), then, when t is odd,
+// NB / 2 "A-shared" ones (the last row tile against block 2w + rank).  So
+// the units of groups [0, g) number NB / 2 * tiles[g], and the row-tile
+// prefix finds a unit's group.
+__device__ __forceinline__ Unit decode_cunit(const Params& p, int v, int rank, int total_tiles,
+                                             const int32_t* s_tiles, const int32_t* s_off, int& a_shared) {
+    Unit r;
+    r.ks = 0;
+    const int H = p.NB >> 1;
+    const int q = v / H;
+    int t0, t;
+    if (p.offsets) {
+        r.g = find_group_smem(s_tiles, p.G, q);
+        t0 = s_tiles[r.g];
+        t = s_tiles[r.g + 1] - t0;
+        r.row0 = s_off[r.g];
+        r.nrows = s_off[r.g + 1] - r.row0;
+    } else {
+        r.g = 0;
+        t0 = 0;
+        t = total_tiles;
+        r.row0 = 0;
+        r.nrows = p.rows;
+    }
+    const int w = v - H * t0;
+    const int b_units = (t >> 1) * p.NB;
+    if (w < b_units) {
+        a_shared = 0;
+        const int q2 = w / p.NB;
+        r.nb = w - q2 * p.NB;
+        r.m0 = (2 * q2 + rank) * BM;
+    } else {
+        a_shared = 1;
+        r.nb = 2 * (w - b_units) + rank;
+        r.m0 = (t - 1) * BM;
+    }
+    return r;
+}
+
 __device__ __forceinline__ void store_f16x32(f16* dst, const float* v) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
@@ -153,12 +204,16 @@ __device__ __forceinline__ void store_bf16x32(bf16* dst, const float* v) {
 
 // ------------------------------------------------------------------ kernel
 
-template <int EPI, bool PAIR>
+// CL: tile pairs on 2-CTA clusters (tm_ah / tm_a_shh: 64-row A boxes; for
+// the plain epilogue tm_b2 then holds 128-row boxes of B).
+template <int EPI, bool PAIR, bool CL>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_sh,
                    const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
                    const __grid_constant__ CUtensorMap tm_af, const __grid_constant__ CUtensorMap tm_a_shf,
+                   const __grid_constant__ CUtensorMap tm_ah, const __grid_constant__ CUtensorMap tm_a_shh,
                    const Params p) {
+    static_assert(!(CL && PAIR), "tile pairs take a single A input");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int kStages = p.stages;
@@ -187,10 +242,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     static_assert((2 * kMaxStages + 13) * 8 + 6 * 4 <= 256, "barrier block overflows");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = CL ? (int)cluster_rank() : 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, CL ? 2 : 1);  // tile pairs: both CTAs' MMAs read what fills it
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(tfull0 + 8 * b, 1);
@@ -212,11 +268,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (CL) cluster_sync();  // the peer's barriers exist before any multicast reaches them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     const int total_tiles = p.offsets ? __ldg(p.tiles + p.g_end) : (p.rows + BM - 1) / BM;
-    const int total_units = total_tiles * p.NB * p.KS;
+    const int total_units = CL ? total_tiles * (p.NB >> 1) : total_tiles * p.NB * p.KS;
     const int kbs = p.KB / p.KS;  // k-blocks per unit
     const int64_t lim = p.spin_ns;
 
@@ -231,11 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // take fewer units) or in the static round-robin order; each is
             // published to the MMA issuer and the epilogue through the unit
             // ring.  The counter is drawn one unit ahead to hide its latency.
-            int next_u = p.sched ? atomicAdd(p.sched, 1) : blockIdx.x;
+            // (tile pairs: both CTAs of a cluster walk the same static order)
+            const int ord0 = CL ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+            const int ordn = CL ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+            int next_u = p.sched ? atomicAdd(p.sched, 1) : ord0;
             for (int i = 0; ok; ++i) {
                 int u = next_u;
                 if (u >= total_units) u = -1;
-                if (u >= 0) next_u = p.sched ? atomicAdd(p.sched, 1) : blockIdx.x + (i + 1) * gridDim.x;
+                if (u >= 0) next_u = p.sched ? atomicAdd(p.sched, 1) : ord0 + (i + 1) * ordn;
                 if (!mbar_wait(uempty0 + 8 * (i & 3), ((i >> 2) & 1) ^ 1, lim, abort_flag)) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 5, blockIdx.x, i);
                     *abort_flag = 1;
@@ -245,13 +305,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s_units[i & 3] = u;
                 mbar_arrive(ufull0 + 8 * (i & 3));
                 if (u < 0) break;
-                const Unit un = decode_unit(p, u, total_tiles, s_tiles, s_off);
+                int a_sh = 0;
+                const Unit un = CL ? decode_cunit(p, u, rank, total_tiles, s_tiles, s_off, a_sh)
+                                   : decode_unit(p, u, total_tiles, s_tiles, s_off);
                 const bool sh = un.g == p.shared_group;
                 const CUtensorMap* ta = sh ? &tm_a_sh : &tm_a;
                 const CUtensorMap* taf = sh ? &tm_a_shf : &tm_af;
+                const CUtensorMap* tah = sh ? &tm_a_shh : &tm_ah;
                 const int a_y = sh ? un.m0 : un.row0 + un.m0;
                 const int valid = min(BM, un.nrows - un.m0);
                 const int nbox = (valid + kBoxRowsA - 1) / kBoxRowsA;
+                // A-shared pair unit: this CTA copies rows [64 rank, 64 rank + 64) of
+                // the tile into both CTAs.  Either way the stage receives the
+                // tile's valid rows in 16-row units plus the whole B tile.
+                const int hv = max(0, min(BM / 2, valid - (BM / 2) * rank));
+                const int hbox = (hv + kBoxRowsA - 1) / kBoxRowsA;
                 const uint32_t bytes = (PAIR ? 2u : 1u) * (uint32_t)nbox * kBoxRowsA * BK * 2 + b_bytes;
                 const int b_y = un.g * p.b_group_rows + un.nb * ((EPI == EPI_SWIGLU) ? 128 : p.BN);
                 for (int kb = un.ks * kbs; kb < (un.ks + 1) * kbs; ++kb) {
@@ -267,7 +335,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                     const uint32_t a_dst = smem_u32(sA + stage * kAStage);
                     const uint32_t b_dst = smem_u32(sB + stage * kBStage);
-                    if (nbox * kBoxRowsA == BM) {  // (nearly) full tile: one 128-row box
+                    if (CL && a_sh) {
+                        const uint32_t h_dst = a_dst + (uint32_t)rank * (kABytes / 2);
+                        const int h_y = a_y + (BM / 2) * rank;
+                        if (hv == BM / 2) {
+                            tma_load_2d_mc(h_dst, tah, fb, kb * BK, h_y, 3);
+                        } else {
+                            for (int i = 0; i < hbox; ++i)
+                                tma_load_2d_mc(h_dst + i * kBoxRowsA * 128, ta, fb, kb * BK, h_y + i * kBoxRowsA, 3);
+                        }
+                    } else if (nbox * kBoxRowsA == BM) {  // (nearly) full tile: one 128-row box
                         tma_load_2d(a_dst, taf, fb, kb * BK, a_y);
                         if (PAIR) tma_load_2d(a_dst + kABytes, taf, fb, p.a_lo_x + kb * BK, a_y);
                     } else {
@@ -279,8 +356,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                     const int bx = kb * BK;
-                    tma_load_2d(b_dst, &tm_b, fb, bx, b_y);
-                    if (EPI == EPI_SWIGLU) tma_load_2d(b_dst + 128 * 128, &tm_b2, fb, bx, b_y);
+                    if (CL && !a_sh) {  // B-shared pair unit: this CTA copies half of the B tile into both
+                        if (EPI == EPI_SWIGLU)
+                            tma_load_2d_mc(b_dst + (uint32_t)rank * (128 * 128), rank ? &tm_b2 : &tm_b, fb, bx, b_y, 3);
+                        else
+                            tma_load_2d_mc(b_dst + (uint32_t)rank * (128 * 128), &tm_b2, fb, bx, b_y + 128 * rank, 3);
+                    } else {
+                        tma_load_2d(b_dst, &tm_b, fb, bx, b_y);
+                        if (EPI == EPI_SWIGLU) tma_load_2d(b_dst + 128 * 128, &tm_b2, fb, bx, b_y);
+                    }
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -293,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         volatile int never = 0;
                         mbar_wait(full0 + 8 * s, (armed_parity >> s) & 1u, 1000000000LL, &never);
                     }
+                if (CL) sleep_ns(200000);  // and the halves it sent to the peer
             }
         }
     } else if (warp == 1) {
@@ -338,7 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int kk = 0; kk < BK / 16; ++kk)
                             umma_bf16(d, al + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, 1u);
                     }
-                    umma_commit(empty0 + 8 * stage);
+                    if (CL) umma_commit_mc(empty0 + 8 * stage, 3);  // the stage was filled by both CTAs
+                    else umma_commit(empty0 + 8 * stage);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1;
@@ -377,7 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             got = __shfl_sync(0xffffffffu, got, 0);
             u = __shfl_sync(0xffffffffu, u, 0);
             if (!got || u < 0) break;
-            const Unit un = decode_unit(p, u, total_tiles, s_tiles, s_off);
+            int a_sh = 0;
+            const Unit un = CL ? decode_cunit(p, u, rank, total_tiles, s_tiles, s_off, a_sh)
+                               : decode_unit(p, u, total_tiles, s_tiles, s_off);
             int ok = 1;
             if (lane == 0) {
                 ok = mbar_wait(tfull0 + 8 * acc, acc_phase, lim, abort_flag);
@@ -487,6 +575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             atomicExch(p.sched + 1, 0);
         }
     }
+    if (CL) cluster_sync();  // no copy or commit of the peer still targets this CTA
 }
 
 // ------------------------------------------------------------------- host
@@ -529,19 +618,59 @@ int plain_bn(int N) {
     return 0;
 }
 
-template <int EPI, bool PAIR>
-cudaError_t launch_one(int grid, const CUtensorMap& ma, const CUtensorMap& msh, const CUtensorMap& mb,
-                       const CUtensorMap& mb2, const CUtensorMap& maf, const CUtensorMap& mshf, const Params& p,
-                       cudaStream_t stream) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<EPI, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kSmemBytes);
+struct Maps {
+    CUtensorMap a, a_sh, b, b2, af, a_shf, ah, a_shh;
+};
+
+// Launch one instantiation.  grid: CTAs for a plain launch; with CL, the
+// upper bound on CTAs (rounded down to whole clusters and capped at the
+// clusters that fit on the GPU at once).
+template <int EPI, bool PAIR, bool CL>
+cudaError_t launch_one(int grid, const Maps& m, const Params& p, cudaStream_t stream) {
+    auto kern = gemm_tc_kernel<EPI, PAIR, CL>;
+    static int ready = 0;  // 0: attributes not set; else (CL) the most co-resident clusters
+    if (!ready) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        attr = true;
+        int n = 1;
+        if (CL) {
+            int dev = 0, sms = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            cudaLaunchConfig_t qc = {};
+            qc.gridDim = dim3(2 * std::max(1, sms / 2));
+            qc.blockDim = dim3(kThreads);
+            qc.dynamicSmemBytes = kSmemBytes;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = 2;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            qc.attrs = qa;
+            qc.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&n, (void*)kern, &qc);
+            if (e != cudaSuccess) return e;
+            if (n < 1) return cudaErrorInvalidConfiguration;
+        }
+        ready = n;
     }
-    gemm_tc_kernel<EPI, PAIR><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, maf, mshf, p);
-    return cudaGetLastError();
+    if (!CL) {
+        kern<<<grid, kThreads, kSmemBytes, stream>>>(m.a, m.a_sh, m.b, m.b2, m.af, m.a_shf, m.ah, m.a_shh, p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * std::max(1, std::min(ready, grid / 2)));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, m.a, m.a_sh, m.b, m.b2, m.af, m.a_shf, m.ah, m.a_shh, p);
 }
 
 }  // namespace tc
@@ -613,31 +742,45 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     p.err = g.err;
     p.spin_ns = g.spin_ns > 0 ? g.spin_ns : 2000000000LL;
 
-    CUtensorMap ma, msh, mb, mb2, maf, mshf;
+    // tile pairs: whole weight blocks in pairs (SwiGLU: 128 gate + 128 up;
+    // plain: 256-wide), no K split, one A input; static unit order
+    const bool cl = g.mcast && !pair && p.KS == 1 && p.NB % 2 == 0 && (sw || p.BN == 256);
+    if (cl) p.sched = nullptr;
+
+    Maps m;
     const int G = g.offsets ? g.G : 1;
-    if (!make_map(&ma, g.a, g.a_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
-    if (!make_map(&maf, g.a, g.a_rows, g.Ka, BM)) return cudaErrorInvalidValue;
+    if (!make_map(&m.a, g.a, g.a_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
+    if (!make_map(&m.af, g.a, g.a_rows, g.Ka, BM)) return cudaErrorInvalidValue;
+    if (cl && !make_map(&m.ah, g.a, g.a_rows, g.Ka, BM / 2)) return cudaErrorInvalidValue;
+    if (!cl) m.ah = m.af;
     if (g.a_shared) {
-        if (!make_map(&msh, g.a_shared, g.a_shared_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
-        if (!make_map(&mshf, g.a_shared, g.a_shared_rows, g.Ka, BM)) return cudaErrorInvalidValue;
+        if (!make_map(&m.a_sh, g.a_shared, g.a_shared_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
+        if (!make_map(&m.a_shf, g.a_shared, g.a_shared_rows, g.Ka, BM)) return cudaErrorInvalidValue;
+        if (cl && !make_map(&m.a_shh, g.a_shared, g.a_shared_rows, g.Ka, BM / 2)) return cudaErrorInvalidValue;
+        if (!cl) m.a_shh = m.a_shf;
     } else {
-        msh = ma;
-        mshf = maf;
+        m.a_sh = m.a;
+        m.a_shf = m.af;
+        m.a_shh = m.ah;
     }
     const int brow_box = sw ? 128 : p.BN;
-    if (!make_map(&mb, g.b, (int64_t)G * g.N, g.Kb, brow_box)) return cudaErrorInvalidValue;
+    if (!make_map(&m.b, g.b, (int64_t)G * g.N, g.Kb, brow_box)) return cudaErrorInvalidValue;
     if (sw) {
-        if (!make_map(&mb2, g.b2, (int64_t)G * g.N, g.Kb, brow_box)) return cudaErrorInvalidValue;
+        if (!make_map(&m.b2, g.b2, (int64_t)G * g.N, g.Kb, brow_box)) return cudaErrorInvalidValue;
+    } else if (cl) {  // halves of the 256-row B tile
+        if (!make_map(&m.b2, g.b, (int64_t)G * g.N, g.Kb, 128)) return cudaErrorInvalidValue;
     } else {
-        mb2 = mb;
+        m.b2 = m.b;
     }
-    const int max_units = g.max_tiles * p.NB * p.KS;
+    const int max_units = cl ? g.max_tiles * (p.NB / 2) * 2 : g.max_tiles * p.NB * p.KS;  // CTAs' worth
     if (max_units <= 0) return cudaGetLastError();
     const int grid = std::max(1, std::min(g.max_ctas > 0 ? std::min(num_sms, g.max_ctas) : num_sms, max_units));
     cudaError_t e;
-    if (sw) e = launch_one<EPI_SWIGLU, false>(grid, ma, msh, mb, mb2, maf, mshf, p, stream);
-    else if (pair) e = launch_one<EPI_PLAIN, true>(grid, ma, msh, mb, mb2, maf, mshf, p, stream);
-    else e = launch_one<EPI_PLAIN, false>(grid, ma, msh, mb, mb2, maf, mshf, p, stream);
+    if (cl && sw) e = launch_one<EPI_SWIGLU, false, true>(grid, m, p, stream);
+    else if (cl) e = launch_one<EPI_PLAIN, false, true>(grid, m, p, stream);
+    else if (sw) e = launch_one<EPI_SWIGLU, false, false>(grid, m, p, stream);
+    else if (pair) e = launch_one<EPI_PLAIN, true, false>(grid, m, p, stream);
+    else e = launch_one<EPI_PLAIN, false, false>(grid, m, p, stream);
     count_launches(1);
     return e;
 }

@@ -36,6 +36,8 @@ struct GroupedGemm {
     int* sched;                  // tensor-core kernels: [2] zeroed device ints for dynamic unit order, or nullptr
     int max_tiles2;              // host bound on the total number of 256-row tiles
     int prefer_pairs;            // 1: run on CTA pairs (M=256) when a kernel for it exists
+    int mcast;                   // bf16/fp16 tensor-core kernel: 1 = tile pairs (2-CTA clusters sharing
+                                 // operand tiles by TMA multicast) where the shape allows them
     int rows;                    // single-group row count
     int max_tiles;               // host bound on the total number of row tiles
     int N;                       // output columns (features) of one group

@@ -195,6 +195,25 @@ __device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols) {
 __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
+// TMA load delivered to the same shared-memory offset in every CTA of the
+// cluster named by `mask` (multicast); the copy's bytes count on the
+// mbarrier at offset `bar` in each of those CTAs.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y,
+                                               uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
+        "{%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+        : "memory");
+}
+// Commit of this thread's (cta_group::1) MMAs, arriving on the mbarrier at
+// offset `bar` in every CTA of the cluster named by `mask`.
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
 // Sleep for about ns nanoseconds (error paths: let copies already in flight land).
 __device__ __forceinline__ void sleep_ns(int64_t ns) {
     const uint64_t t0 = globaltimer_ns();

@@ -100,8 +100,8 @@ def test_small_fp32_ragged(T):
 
 
 @pytest.mark.parametrize("flags", [0, L.MOE_FLAG_FORCE_SIMT, L.MOE_FLAG_PAIR_CTA_ON, L.MOE_FLAG_DOWN_HILO,
-                                   L.MOE_FLAG_DOWN_HILO | L.MOE_FLAG_FORCE_SIMT],
-                         ids=["default", "simt", "cta_pairs", "hilo", "hilo_simt"])
+                                   L.MOE_FLAG_DOWN_HILO | L.MOE_FLAG_FORCE_SIMT, L.MOE_FLAG_MCAST_ON],
+                         ids=["default", "simt", "cta_pairs", "hilo", "hilo_simt", "tile_pairs"])
 @pytest.mark.parametrize("T", [300, 1, 128, 129, 700])
 def test_small_bf16_layer(flags, T):
     shape = synth.SMALL_BF16.with_tokens(T)
@@ -211,6 +211,26 @@ def test_forward_equals_stage_pipeline(shape, T):
     torch.cuda.synchronize()
     layer.check()
     assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("T", [700, 300, 129, 1])
+def test_tile_pairs_bit_identical(T):
+    """Tile pairs (2-CTA clusters sharing A or B tiles by TMA multicast)
+    change only where the operands come from: every output tile sees the same
+    MMAs in the same order, so the layer output and the expert outputs equal
+    the single-CTA kernel's bit for bit."""
+    shape = synth.SMALL_BF16.with_tokens(T)
+    inp = _dev_inputs(shape, seed=16)
+    on = MoELayer.from_shape(shape, inp, flags=L.MOE_FLAG_MCAST_ON)
+    off = MoELayer.from_shape(shape, inp, flags=L.MOE_FLAG_MCAST_OFF)
+    a = on.forward(inp["x"]).clone()
+    b = off.forward(inp["x"]).clone()
+    torch.cuda.synchronize()
+    on.check()
+    off.check()
+    assert torch.equal(a, b)
+    va, vb = on.views(T), off.views(T)
+    assert torch.equal(va["h"], vb["h"]) and torch.equal(va["y"], vb["y"])
 
 
 def test_forward_into_mapped_host_memory():
@@ -428,8 +448,11 @@ def big_bf16_weights():
 
 
 @pytest.mark.parametrize("shape,flags", [(synth.DECODE_BF16, 0), (synth.BATCHED_DECODE_BF16, 0),
-                                         (synth.PREFILL_BF16, 0), (synth.PREFILL_BF16, L.MOE_FLAG_PAIR_CTA_ON)],
-                         ids=["decode", "batched_decode", "prefill", "prefill_cta_pairs"])
+                                         (synth.PREFILL_BF16, 0), (synth.PREFILL_BF16, L.MOE_FLAG_PAIR_CTA_ON),
+                                         (synth.PREFILL_BF16, L.MOE_FLAG_MCAST_OFF),
+                                         (synth.BATCHED_DECODE_BF16, L.MOE_FLAG_MCAST_ON)],
+                         ids=["decode", "batched_decode", "prefill", "prefill_cta_pairs", "prefill_no_tile_pairs",
+                              "batched_decode_tile_pairs"])
 def test_full_size_bf16_workloads(shape, flags, big_bf16_weights):
     inp = _dev_inputs(shape, seed=0, weights=False)
     inp.update(big_bf16_weights)
