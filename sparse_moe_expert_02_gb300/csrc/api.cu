@@ -483,7 +483,7 @@ moe::GroupedGemm down_gemm(const moe_plan* p, const moe_weights* w, int32_t T, W
     // dynamic unit order measured slower for the bf16 down GEMM (0.80 vs
     // 0.78 ms at T=8192), faster for the FP8 one (1.42 vs 1.43 ms) and for
     // every gate/up GEMM
-    g.sched = fp8 ? W.sched(kSchedDown) : nullptr;
+    g.sched = W.sched(kSchedDown);  // (tile pairs at prefill take the static order)
     g.spin_ns = p->spin_ns;
     return g;
 }
