@@ -112,6 +112,15 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2 } moe_
  * T * top_k >= 64 * E (at least 64 rows per expert on average: prefill). */
 #define MOE_FLAG_MCAST_ON 0x10u    /* tile pairs whenever the shape allows them */
 #define MOE_FLAG_MCAST_OFF 0x20u   /* never tile pairs */
+/* Narrow tails: in the bf16 layer's tensor-core expert GEMMs a tile with at
+ * most 112 valid rows (a group's ragged last tile, every tile at decode
+ * sizes) is multiplied transposed, weights as the MMA's 128-wide side and the
+ * rows as its N side rounded up to 16, so padding rows cost no tensor time.
+ * By default only the gate/up GEMM uses them, and only where tile pairs are
+ * on (T * top_k >= 64 * E); the down GEMM's transposed stores of y cost more
+ * than the MMA time saved. */
+#define MOE_FLAG_NARROW_TAILS_ON 0x40u   /* narrow tails in both expert GEMMs at every size */
+#define MOE_FLAG_NARROW_TAILS_OFF 0x80u  /* every tile as 128 rows x N features */
 
 typedef struct moe_config {
     int32_t T_max;           /* largest token count a call may pass */

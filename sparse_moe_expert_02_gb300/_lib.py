@@ -30,6 +30,8 @@ MOE_FLAG_PAIR_CTA_ON = 0x4
 MOE_FLAG_DOWN_HILO = 0x8
 MOE_FLAG_MCAST_ON = 0x10
 MOE_FLAG_MCAST_OFF = 0x20
+MOE_FLAG_NARROW_TAILS_ON = 0x40
+MOE_FLAG_NARROW_TAILS_OFF = 0x80
 
 DTYPE_CODE = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8": MOE_FP8_E4M3_B128}
 

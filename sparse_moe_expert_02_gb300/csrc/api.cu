@@ -188,6 +188,17 @@ int prefer_mcast(const moe_plan* p, int T) {
     return (int64_t)T * p->cfg.top_k >= 64 * (int64_t)p->cfg.E ? 1 : 0;
 }
 
+// Narrow tails save tensor time on ragged tiles; measured at T=8192 they
+// take the gate/up GEMM from 1.264 to 1.247 ms, while in the down GEMM (y
+// stored transposed, 2 bytes at a time) and at decode sizes they cost more
+// than they save.
+int prefer_narrow(const moe_plan* p, int T, bool gateup) {
+    const uint32_t f = p->cfg.flags;
+    if (f & MOE_FLAG_NARROW_TAILS_OFF) return 0;
+    if (f & MOE_FLAG_NARROW_TAILS_ON) return 1;
+    return gateup && prefer_mcast(p, T) ? 1 : 0;
+}
+
 int grouped_max_tiles2(const moe_config& c, int T) {
     const int64_t R = (int64_t)T * (c.top_k + 1);
     return (int)(R / (2 * moe::kRowTile) + c.E + 2);
@@ -425,6 +436,7 @@ moe::GroupedGemm gateup_gemm(const moe_plan* p, const moe_weights* w, const void
     g.max_tiles2 = grouped_max_tiles2(c, T);
     g.prefer_pairs = prefer_pairs(p, T);
     g.mcast = prefer_mcast(p, T);
+    g.narrow = prefer_narrow(p, T, true);
     g.N = c.I;
     g.Ka = g.Kb = c.D;
     g.out_pair = hilo(c);
@@ -462,6 +474,7 @@ moe::GroupedGemm down_gemm(const moe_plan* p, const moe_weights* w, int32_t T, W
     g.max_tiles2 = grouped_max_tiles2(c, T);
     g.prefer_pairs = prefer_pairs(p, T);
     g.mcast = prefer_mcast(p, T);
+    g.narrow = prefer_narrow(p, T, false);
     g.N = c.D;
     g.Kb = c.I;
     g.Ka = hilo(c) ? 2 * c.I : c.I;  // the hi/lo pair walks W_down twice

@@ -36,6 +36,14 @@
 // stay 128 rows, so no padding is added.  Each CTA's stage is written by both
 // CTAs, so both MMA issuers' commits release it (commit multicast), and the
 // cluster synchronises before it exits.
+// Narrow tails (where enabled): a unit whose tile holds at most 112 valid
+// rows (a group's ragged last tile; every tile at decode sizes) is
+// multiplied transposed:
+// the weight rows are the MMA's M = 128 side (one MMA per 128 features) and
+// the tile's rows its N side, rounded up to 16, so the tensor pipe spends
+// time in proportion to the rows that exist instead of on 128.  The stage
+// holds the same operands either way; the epilogue then reads a feature per
+// TMEM lane and a row per column.
 // Operands are K-major with the 128-byte swizzle on both sides (TMA writes
 // it, the UMMA descriptor reads it).  Every mbarrier wait is bounded by
 // spin_ns; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its
@@ -59,6 +67,7 @@ constexpr int kABytes = BM * BK * 2;      // 16 KB: one A tile
 constexpr int kBBytesMax = 256 * BK * 2;  // 32 KB
 constexpr int kThreads = 192;
 constexpr int kAccCols = 256;             // TMEM columns per accumulator buffer
+constexpr int kNarrowMax = 112;           // narrow-tail units: at most this many valid rows
 constexpr int kBoxRowsA = 16;             // a ragged tile's A rows come in 16-row boxes (2 KB);
                                           // a full tile's in one 128-row box: the single
                                           // producer thread issues few TMA instructions
@@ -101,6 +110,7 @@ struct Params {
     int out_f32;
     int out_f16;         // SwiGLU output as fp16 (single rounding) instead of bf16
     int in_f16;          // A and B are fp16 (else bf16)
+    int narrow;          // units of <= kNarrowMax valid rows run transposed (narrow tails)
     int stages;          // ring depth (<= kMaxStages)
     int b_stage;         // bytes of one B stage
     void* out;
@@ -396,6 +406,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int u = s_units[i & 3];
                 mbar_arrive(uempty0 + 8 * (i & 3));
                 if (u < 0) break;
+                int nn = 0;  // narrow tail: N of the transposed MMAs (valid rows rounded up to 16), else 0
+                if (p.narrow) {
+                    int a_sh = 0;
+                    const Unit un = CL ? decode_cunit(p, u, rank, total_tiles, s_tiles, s_off, a_sh)
+                                       : decode_unit(p, u, total_tiles, s_tiles, s_off);
+                    const int valid = min(BM, un.nrows - un.m0);
+                    if (valid <= kNarrowMax) nn = (valid + 15) & ~15;
+                }
+                const uint32_t idesc_n = p.in_f16 ? idesc_f16(BM, nn > 0 ? nn : 16) : idesc_bf16(BM, nn > 0 ? nn : 16);
+                const int regions = (EPI == EPI_SWIGLU) ? 2 : p.BN / 128;
                 if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, lim, abort_flag)) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 2, blockIdx.x, u);
                     *abort_flag = 1;
@@ -414,9 +434,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint64_t ad = umma_desc(smem_u32(sA + stage * kAStage));
                     const uint64_t bd = umma_desc(smem_u32(sB + stage * kBStage));
+                    if (nn > 0) {
+                        // transposed: weight rows [128 r, 128 r + 128) of the B tile as M, the
+                        // tile's rows as N; region r accumulates at TMEM columns [128 r, ...)
+                        for (int r = 0; r < regions; ++r) {
+                            const uint64_t wd = umma_desc(smem_u32(sB + stage * kBStage + r * kABytes));
 #pragma unroll
-                    for (int kk = 0; kk < BK / 16; ++kk)  // K=16 per MMA: 32 bytes along the swizzled row
-                        umma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                            for (int kk = 0; kk < BK / 16; ++kk)
+                                umma_bf16(d + (uint32_t)(r * 128), wd + (uint64_t)(kk * 2), ad + (uint64_t)(kk * 2),
+                                          idesc_n, (kb | kk) != 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)  // K=16 per MMA: 32 bytes along the swizzled row
+                            umma_bf16(d, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), idesc, (kb | kk) != 0);
+                    }
                     if (PAIR) {
                         const uint64_t al = umma_desc(smem_u32(sA + stage * kAStage + kABytes));
 #pragma unroll
@@ -481,7 +513,61 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = m < un.nrows;
             const int64_t orow = (int64_t)un.row0 + m;
             const uint32_t tb = tmem_base + ((uint32_t)(sub * 32) << 16) + (uint32_t)(acc * kAccCols);
-            if (EPI == EPI_SWIGLU) {
+            const int nvalid = min(BM, un.nrows - un.m0);
+            if (p.narrow && nvalid <= kNarrowMax) {
+                // narrow tail: this thread holds feature `row` of each 128-feature
+                // region, one tile row per TMEM column
+                const int64_t orow0 = (int64_t)un.row0 + un.m0;
+                if (EPI == EPI_SWIGLU) {
+                    f16* o = (f16*)p.out + orow0 * p.ldo + un.nb * 128 + row;
+                    bf16* ob = (bf16*)p.out + orow0 * p.ldo + un.nb * 128 + row;
+                    float mx = 0.f;
+#pragma unroll 1
+                    for (int c = 0; c < nvalid; c += 32) {
+                        uint32_t gr[32], ur[32];
+                        tmem_ld32(tb + c, gr);
+                        tmem_ld32(tb + 128 + c, ur);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (c + i < nvalid) {
+                                const float h = swiglu(__uint_as_float(gr[i]), __uint_as_float(ur[i]));
+                                if (p.out_f16) {
+                                    mx = fmaxf(mx, fabsf(h));
+                                    o[(int64_t)(c + i) * p.ldo] = __float2half_rn(h);
+                                } else {
+                                    ob[(int64_t)(c + i) * p.ldo] = __float2bfloat16_rn(h);
+                                }
+                            }
+                    }
+                    if (p.out_f16 && !(mx <= 65504.f)) record_error(p.err, MOE_ERR_NONFINITE, 5, blockIdx.x, 0);
+                } else {
+                    float mx = 0.f;
+#pragma unroll 1
+                    for (int r = 0; r < p.BN / 128; ++r) {
+                        const int64_t col = (int64_t)un.nb * p.BN + r * 128 + row;
+#pragma unroll 1
+                        for (int c = 0; c < nvalid; c += 32) {
+                            uint32_t v[32];
+                            tmem_ld32(tb + r * 128 + c, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                if (c + i < nvalid) {
+                                    const float y = __uint_as_float(v[i]);
+                                    const int64_t at = (orow0 + c + i) * p.ldo + col;
+                                    if (p.out_f16) {
+                                        mx = fmaxf(mx, fabsf(y));
+                                        ((f16*)p.out)[at] = __float2half_rn(y);
+                                    } else {
+                                        ((bf16*)p.out)[at] = __float2bfloat16_rn(y);
+                                    }
+                                }
+                        }
+                    }
+                    if (p.out_f16 && !(mx <= 65504.f)) record_error(p.err, MOE_ERR_NONFINITE, 6, blockIdx.x, 0);
+                }
+            } else if (EPI == EPI_SWIGLU) {
                 bf16* o = (bf16*)p.out + orow * p.ldo + un.nb * 128;
 #pragma unroll 1
                 for (int c = 0; c < 128; c += 32) {
@@ -746,6 +832,9 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     // plain: 256-wide), no K split, one A input; static unit order
     const bool cl = g.mcast && !pair && p.KS == 1 && p.NB % 2 == 0 && (sw || p.BN == 256);
     if (cl) p.sched = nullptr;
+    // narrow tails: expert GEMMs with 16-bit outputs in whole 128-feature regions
+    p.narrow = g.narrow && !pair && p.KS == 1 && !g.out_pair && !g.bias && g.out_elem != kF32 &&
+               (sw || p.BN % 128 == 0);
 
     Maps m;
     const int G = g.offsets ? g.G : 1;

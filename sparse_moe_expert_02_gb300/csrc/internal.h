@@ -38,6 +38,8 @@ struct GroupedGemm {
     int prefer_pairs;            // 1: run on CTA pairs (M=256) when a kernel for it exists
     int mcast;                   // bf16/fp16 tensor-core kernel: 1 = tile pairs (2-CTA clusters sharing
                                  // operand tiles by TMA multicast) where the shape allows them
+    int narrow;                  // bf16/fp16 tensor-core kernel: 1 = tiles of <= 112 valid rows multiplied
+                                 // transposed (weights as M, rows as N rounded up to 16)
     int rows;                    // single-group row count
     int max_tiles;               // host bound on the total number of row tiles
     int N;                       // output columns (features) of one group

@@ -100,8 +100,10 @@ def test_small_fp32_ragged(T):
 
 
 @pytest.mark.parametrize("flags", [0, L.MOE_FLAG_FORCE_SIMT, L.MOE_FLAG_PAIR_CTA_ON, L.MOE_FLAG_DOWN_HILO,
-                                   L.MOE_FLAG_DOWN_HILO | L.MOE_FLAG_FORCE_SIMT, L.MOE_FLAG_MCAST_ON],
-                         ids=["default", "simt", "cta_pairs", "hilo", "hilo_simt", "tile_pairs"])
+                                   L.MOE_FLAG_DOWN_HILO | L.MOE_FLAG_FORCE_SIMT, L.MOE_FLAG_MCAST_ON,
+                                   L.MOE_FLAG_NARROW_TAILS_ON, L.MOE_FLAG_NARROW_TAILS_ON | L.MOE_FLAG_MCAST_ON],
+                         ids=["default", "simt", "cta_pairs", "hilo", "hilo_simt", "tile_pairs", "narrow_tails",
+                              "narrow_tails_tile_pairs"])
 @pytest.mark.parametrize("T", [300, 1, 128, 129, 700])
 def test_small_bf16_layer(flags, T):
     shape = synth.SMALL_BF16.with_tokens(T)
@@ -355,13 +357,14 @@ def test_nonfinite_logit_is_reported():
     assert L.moe_check_status(layer.plan, layer.ws) == L.MOE_ERR_NONFINITE
 
 
-def test_bf16_fp16_h_overflow_is_reported():
+@pytest.mark.parametrize("flags", [0, L.MOE_FLAG_NARROW_TAILS_ON], ids=["default", "narrow_tails"])
+def test_bf16_fp16_h_overflow_is_reported(flags):
     """fp16 h holds |h| <= 65504: beyond that the layer reports, and the
     hi/lo pair path (no range limit) still matches the oracle."""
     shape = synth.SMALL_BF16.with_tokens(64)
     inp = _dev_inputs(shape, seed=7)
     inp["x"] = (inp["x"].float() * 400.0).to(torch.bfloat16)
-    layer = MoELayer.from_shape(shape, inp)
+    layer = MoELayer.from_shape(shape, inp, flags=flags)
     layer.forward(inp["x"])
     assert L.moe_check_status(layer.plan, layer.ws) == L.MOE_ERR_NONFINITE
     assert int(layer.views(64)["err"][1]) == 5
@@ -450,9 +453,11 @@ def big_bf16_weights():
 @pytest.mark.parametrize("shape,flags", [(synth.DECODE_BF16, 0), (synth.BATCHED_DECODE_BF16, 0),
                                          (synth.PREFILL_BF16, 0), (synth.PREFILL_BF16, L.MOE_FLAG_PAIR_CTA_ON),
                                          (synth.PREFILL_BF16, L.MOE_FLAG_MCAST_OFF),
-                                         (synth.BATCHED_DECODE_BF16, L.MOE_FLAG_MCAST_ON)],
+                                         (synth.BATCHED_DECODE_BF16, L.MOE_FLAG_MCAST_ON),
+                                         (synth.PREFILL_BF16, L.MOE_FLAG_NARROW_TAILS_OFF),
+                                         (synth.DECODE_BF16, L.MOE_FLAG_NARROW_TAILS_ON)],
                          ids=["decode", "batched_decode", "prefill", "prefill_cta_pairs", "prefill_no_tile_pairs",
-                              "batched_decode_tile_pairs"])
+                              "batched_decode_tile_pairs", "prefill_wide_tails", "decode_narrow_tails"])
 def test_full_size_bf16_workloads(shape, flags, big_bf16_weights):
     inp = _dev_inputs(shape, seed=0, weights=False)
     inp.update(big_bf16_weights)
