@@ -23,6 +23,18 @@ def test_header_declarations_match_binding():
     assert decl == sorted(L.SYMBOLS)
 
 
+def test_header_flags_match_binding():
+    """Every MOE_FLAG_* bit of the header has the same value in the binding,
+    and no two flags share a bit."""
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    flags = {n: int(v, 16) for n, v in re.findall(r"^#define\s+(MOE_FLAG_\w+)\s+(0x[0-9a-fA-F]+)u", text, re.M)}
+    assert len(flags) >= 8
+    for n, v in flags.items():
+        assert getattr(L, n) == v, n
+        assert v & (v - 1) == 0, n
+    assert len(set(flags.values())) == len(flags)
+
+
 def test_library_exports_every_declared_symbol():
     path = B.build()
     out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True, check=True).stdout
