@@ -38,12 +38,11 @@
 // cluster synchronises before it exits.
 // Narrow tails (where enabled): a unit whose tile holds at most 112 valid
 // rows (a group's ragged last tile; every tile at decode sizes) is
-// multiplied transposed:
-// the weight rows are the MMA's M = 128 side (one MMA per 128 features) and
-// the tile's rows its N side, rounded up to 16, so the tensor pipe spends
-// time in proportion to the rows that exist instead of on 128.  The stage
-// holds the same operands either way; the epilogue then reads a feature per
-// TMEM lane and a row per column.
+// multiplied transposed: the weight rows are the MMA's M = 128 side (one MMA
+// per 128 features) and the tile's rows its N side, rounded up to 16, so the
+// tensor pipe spends time in proportion to the rows that exist instead of on
+// 128.  The stage holds the same operands either way; the epilogue then
+// reads a feature per TMEM lane and a row per column.
 // Operands are K-major with the 128-byte swizzle on both sides (TMA writes
 // it, the UMMA descriptor reads it).  Every mbarrier wait is bounded by
 // spin_ns; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT, drains its
@@ -414,7 +413,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int valid = min(BM, un.nrows - un.m0);
                     if (valid <= kNarrowMax) nn = (valid + 15) & ~15;
                 }
-                const uint32_t idesc_n = p.in_f16 ? idesc_f16(BM, nn > 0 ? nn : 16) : idesc_bf16(BM, nn > 0 ? nn : 16);
+                const int n_t = nn > 0 ? nn : 16;
+                const uint32_t idesc_n = p.in_f16 ? idesc_f16(BM, n_t) : idesc_bf16(BM, n_t);
                 const int regions = (EPI == EPI_SWIGLU) ? 2 : p.BN / 128;
                 if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, lim, abort_flag)) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 2, blockIdx.x, u);
