@@ -207,7 +207,8 @@ MOE_API moe_status moe_quantize_weights(const moe_plan* plan, const float* w, in
 
 /* The whole layer: route, permute, gate/up GEMM with SwiGLU, down GEMM,
  * unpermute with the shared-expert add.  x [T, D] (fp32 for MOE_F32, else
- * bf16); out [T, D] of cfg.out_dtype.  blob_out (nullable) receives a copy of
+ * bf16); out [T, D] of cfg.out_dtype; 1 <= T <= T_max, or T = 0 (an empty
+ * batch: MOE_OK at once, no pointer is read and nothing is launched).  blob_out (nullable) receives a copy of
  * the [2, T, top_k] routing blob; logits_out (nullable) a copy of the [T, E]
  * fp32 logits.  Clears the workspace error word first.
  * On the tensor-core paths (bf16 and FP8; not MOE_FLAG_FORCE_SIMT or

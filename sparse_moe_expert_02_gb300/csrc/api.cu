@@ -576,6 +576,7 @@ moe_status moe_unpermute(const moe_plan* p, int32_t T, void* out, void* ws, size
 
 moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, void* out,
                        int32_t* blob_out, float* logits_out, void* ws, size_t ws_bytes, void* stream) {
+    if (p && T == 0) return MOE_OK;  // an empty batch: nothing to read, write or launch
     Ws W;
     moe_status st = check_call(p, T, ws, ws_bytes, &W);
     if (st != MOE_OK) return st;

@@ -399,6 +399,24 @@ def test_host_argument_errors():
     with pytest.raises(L.MoEError) as e:                 # workspace too small
         L.moe_forward(layer.plan, layer.cw, x, 64, layer.new_out(64), None, None, layer.ws[:4096])
     assert e.value.status == L.MOE_ERR_WORKSPACE
+    with pytest.raises(L.MoEError) as e:                 # stage calls take 1 <= T <= T_max
+        L.moe_route(layer.plan, layer.cw, x, 0, layer.ws)
+    assert e.value.status == L.MOE_ERR_INVALID_ARG
+
+
+def test_empty_batch_is_a_no_op():
+    """T = 0: moe_forward returns at once and launches nothing; the layer
+    then runs a real batch as usual."""
+    shape = synth.SMALL_BF16.with_tokens(64)
+    inp = _dev_inputs(shape, seed=8)
+    layer = MoELayer.from_shape(shape, inp)
+    n0 = L.moe_launch_count()
+    out = layer.forward(inp["x"][:0])
+    assert out.shape == (0, shape.D)
+    assert L.moe_launch_count() == n0
+    ref = MoELayer.from_shape(shape, inp).forward(inp["x"])
+    assert torch.equal(layer.forward(inp["x"]), ref)
+    layer.check()
 
 
 # ------------------------------------------------------------- FP8 layer
