@@ -18,6 +18,11 @@ Parity status per function (what pins each one, see ``oracle.c`` header):
                            beyond those invariants, parity unpinned.
   orc_quant_blocks         pinned: block-amax definition on planted blocks,
                            codes vs torch.float8_e4m3fn.
+  quant_row_128            pinned: per-row, per-128-column amax/448 against
+  (orc_quant_rows_128)     torch.float8_e4m3fn, group amaxes over four
+                           decades, an all-zero group, exact E4M3 ties; and
+                           in place in the FP8 layer (E = 1, k = 1 against a
+                           numpy pipeline over the same torch quantiser).
 """
 from __future__ import annotations
 
@@ -69,6 +74,7 @@ def lib():
             L.orc_e4m3_encode_array.argtypes = [I64, P, P]
             L.orc_bf16_encode_array.argtypes = [I64, P, P]
             L.orc_quant_blocks.argtypes = [I64, I64, I64, I64, P, P, P]
+            L.orc_quant_rows_128.argtypes = [I64, I64, P, P]
             L.orc_logits.argtypes = [I64, I32, I32, I32, P, I32, P, P, P]
             L.orc_topk.argtypes = [I64, I32, I32, P, P, P]
             L.orc_permute.argtypes = [I64, I32, I32, P, P, P, P, P]
@@ -137,6 +143,16 @@ def quant_blocks(w: np.ndarray, br: int, bc: int):
     # blocks never straddle two leading slices because rows % br == 0
     lib().orc_quant_blocks(lead * rows, cols, br, bc, _p(w2), _p(q), _p(s))
     return q, s
+
+
+def quant_rows_128(v: np.ndarray) -> np.ndarray:
+    """The FP8 layer's activation quantiser (per row, per 128 columns) as
+    the doubles its codes stand for (code * scale)."""
+    v = _c(v, np.float32)
+    rows, cols = v.shape
+    deq = np.empty((rows, cols), np.float64)
+    lib().orc_quant_rows_128(rows, cols, _p(v), _p(deq))
+    return deq
 
 
 def logits(x, w_r, bias=None) -> np.ndarray:

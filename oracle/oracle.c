@@ -31,7 +31,9 @@
  * mixture; E = 1, k = 1 reproduces a dense SwiGLU FFN computed with numpy;
  * identity experts make permute-then-unpermute the identity; counts sum to
  * T*k and the permutation is a bijection; token-order equivariance and
- * expert relabelling invariance.  The whole-layer output has no worked value
+ * expert relabelling invariance; the 128x128 weight-block and the per-row
+ * 128-column activation quantisers against torch's E4M3 cast, and the FP8
+ * layer with one expert against numpy over that cast.  The whole-layer output has no worked value
  * in the pages: beyond these invariants it is parity unpinned.
  */
 #include <math.h>
@@ -166,6 +168,12 @@ static void quant_row_128(int64_t n, const float* v, double* deq) {
             deq[c] = orc_e4m3_to_f64(orc_f32_to_e4m3(p)) * (double)scale;
         }
     }
+}
+
+/* Rows of activations through quant_row_128, one row at a time (exported so
+ * that the tests can pin the quantiser itself). */
+ORC_EXPORT void orc_quant_rows_128(int64_t rows, int64_t cols, const float* v, double* deq) {
+    for (int64_t r = 0; r < rows; ++r) quant_row_128(cols, v + r * cols, deq + r * cols);
 }
 
 /* ----------------------------------------------------------------- router */

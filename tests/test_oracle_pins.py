@@ -96,6 +96,83 @@ def test_quant_blocks_definition():
     assert np.all(np.abs(deq - w)[nz] <= np.abs(w)[nz] * 2.0 ** -4 + 1e-12)
 
 
+def _torch_quant_row_128(v, width=128):
+    """Independent per-row, per-128-column E4M3 quantiser (torch's cast),
+    returned as code value * scale: s = amax/448, code = e4m3(fp32(v * fp32(448/amax))),
+    an all-zero group keeps scale 1.  (`width` only serves to build the
+    wrong variants the pin must tell apart.)"""
+    v = np.asarray(v, np.float32)
+    rows, cols = v.shape
+    out = np.empty((rows, cols), np.float64)
+    for c0 in range(0, cols, width):
+        grp = v[:, c0:c0 + width]
+        amax = np.abs(grp).max(axis=1).astype(np.float32)
+        zero = amax == 0
+        a = np.where(zero, np.float32(1), amax).astype(np.float32)
+        scale = np.where(zero, np.float32(1), (a / np.float32(448)).astype(np.float32)).astype(np.float32)
+        inv = np.where(zero, np.float32(1), (np.float32(448) / a).astype(np.float32)).astype(np.float32)
+        p = (grp * inv[:, None]).astype(np.float32)
+        codes = torch.from_numpy(p).to(torch.float8_e4m3fn).double().numpy()
+        out[:, c0:c0 + width] = codes * scale.astype(np.float64)[:, None]
+    return out
+
+
+def test_quant_row_128_definition():
+    """The FP8 layer's activation quantiser (x before the gate/up GEMM, h
+    before the down GEMM): one scale per row and 128 columns.  Groups whose
+    amax spans four decades, an all-zero group and exact E4M3 ties make a
+    group width of 256, a whole-row amax or a wrong tie rule fail."""
+    g = np.random.default_rng(21)
+    rows, cols = 6, 768
+    v = g.normal(0, 1, (rows, cols)).astype(np.float32)
+    decades = np.array([1e-3, 1e-1, 1e1, 1e-2, 1.0, 1e2], np.float32)
+    for r in range(rows):
+        v[r] *= np.repeat(np.roll(decades, r), 128)
+    v[2, 256:384] = 0.0                                   # an all-zero group
+    # a group with amax exactly 448 (scale 1): E4M3 midpoints tie to even
+    grid = oracle.e4m3_decode(np.arange(0x38, 0x50, dtype=np.uint8))
+    mids = ((grid[:-1] + grid[1:]) / 2).astype(np.float32)
+    v[4, 128:128 + len(mids)] = mids
+    v[4, 128 + len(mids):256] = 0.25
+    v[4, 255] = 448.0
+    got = oracle.quant_rows_128(v)
+    ref = _torch_quant_row_128(v)
+    assert np.array_equal(got, ref)
+    assert (got[2, 256:384] == 0).all()
+    codes_mid = oracle.e4m3_encode(mids)
+    assert np.array_equal(got[4, 128:128 + len(mids)], oracle.e4m3_decode(codes_mid))
+    assert (codes_mid % 2 == 0).all()
+    # the plausible slips give different values on these rows
+    for width in (256, cols):                    # 256-wide groups; one amax per row
+        assert (_torch_quant_row_128(v, width) != got).mean() > 0.25
+
+
+def test_fp8_single_expert_layer_quantises_x_and_h_per_128_group():
+    """E = 1, k = 1 FP8 layer: x is quantised per token per 128 columns
+    before the gate/up projections and h (rounded to fp32) before the down
+    projection, weights are the 128x128 block codes times their scales.
+    Checked against numpy matmuls over torch's E4M3 cast."""
+    shape = synth.LayerShape("t", 5, 256, 1, 256, 1, "fp8")
+    inp = synth.make_inputs(shape, seed=22)
+    exq = oracle.Experts.quantised(inp["w_gate"], inp["w_up"], inp["w_down"])
+    x = inp["x"]
+    out, y = oracle.moe_tokens(x, np.zeros((5, 1), np.int32), np.ones((5, 1)), exq, want_y=True)
+
+    def deq(q, s):
+        return oracle.e4m3_decode(q) * np.repeat(np.repeat(s.astype(np.float64), 128, 0), 128, 1)
+
+    xd = _torch_quant_row_128(x.float().numpy())
+    ref = np.zeros((5, 256))
+    for grp in range(2):
+        a = xd @ deq(exq.wg[grp], exq.sg[grp]).T
+        u = xd @ deq(exq.wu[grp], exq.su[grp]).T
+        h = (a / (1 + np.exp(-a)) * u).astype(np.float32)
+        yg = _torch_quant_row_128(h) @ deq(exq.wd[grp], exq.sd[grp]).T
+        assert np.allclose(y[:, 0 if grp == 0 else 1], yg, rtol=1e-12, atol=1e-12)
+        ref += yg
+    assert np.allclose(out, ref, rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------- routing
 
 def _brute_topk(z, k):
