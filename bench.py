@@ -1,7 +1,7 @@
 """Benchmark of the routed-MoE FFN layer on GB300 (one JSON line on stdout).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--no-cpu-baseline]
+    python bench.py [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-cpu-baseline] [--no-extra-workloads]
 
 A step is one pass of the whole layer (router + top-k, permutation, gate/up
 GEMM with SwiGLU, down GEMM, unpermutation with the shared expert) over one
@@ -11,14 +11,17 @@ one shared expert, bf16).  A timed step is one moe_forward call on
 device-resident x and out; a second pass through the stage entry points,
 with events between stages, gives the per-stage times and the dominant
 kernel's roofline.  Expert weights (12.9 GB) dwarf the 129 MB L2, so no
-flush is needed between steps.  With N > 1 (torchrun) every rank runs an
-independent replica of the layer on its own GPU (the layer needs no
-exchange); `value` counts the tokens of all ranks over the slowest rank's
-time.
+flush is needed between steps.  The default run then times the batched
+decode, prefill bf16 and FP8 prefill workloads the same way and reports
+them under "workloads".
+
+Our arm runs on one GPU: the layer shards nothing, and a launch with
+WORLD_SIZE > 1 is refused before the library is loaded.
 
 --impl reference times the fp64 CPU oracle on the host cores instead (a
 bounded sample of the workload per step); it is the baseline the pages'
-method is checked against, not a target.
+method is checked against, not a target.  Under torchrun (gloo) rank 0
+alone runs it.
 """
 from __future__ import annotations
 
@@ -165,7 +168,28 @@ def traffic_for(kernel: str, workload: str):
 
 # ------------------------------------------------------------------ ours
 
-def run_ours(args, shape, world, rank, local):
+def binding_roof(bytes_, flops, ms, shape, peaks, f32_hbm=True):
+    """Roofline of a kernel or of the layer against whichever ceiling binds:
+    its algorithmic bytes at the HBM copy bandwidth, or its algorithmic flops
+    at the dense tensor peak of its dtype (the sustained figure: it runs
+    inside a long step; FP8 = 2x bf16, the nominal dense ratio)."""
+    tc_peak = (peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]) * (2.0 if shape.dtype == "fp8" else 1.0)
+    t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (tc_peak * 1e12)
+    if (f32_hbm and shape.dtype == "f32") or t_hbm >= t_tc:
+        achieved = bytes_ / (ms / 1e3) / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4)}
+    achieved = flops / (ms / 1e3) / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
+            "frac": round(achieved / tc_peak, 4),
+            "peak_note": ("fp8 = 2 x measured bf16 sustained (nominal dense ratio)" if shape.dtype == "fp8"
+                          else "measured bf16 sustained")}
+
+
+def run_ours(args, shape, local, e2e=True):
+    """One workload on this process's GPU: the timed moe_forward steps, the
+    per-stage pass, and (e2e) the end-to-end pass through host buffers."""
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     inp = synth.make_inputs(shape, seed=args.seed, device=dev)
@@ -181,8 +205,6 @@ def run_ours(args, shape, world, rank, local):
     alg = algorithmic(shape, counts)
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)] for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         time.sleep(0.3)  # let nvidia-smi start sampling
@@ -219,22 +241,59 @@ def run_ours(args, shape, world, rank, local):
         torch.cuda.synchronize(dev)
         clk.mark("t_end")
     layer.check()
-    ms_local = t_start.elapsed_time(t_end)
+    ms = t_start.elapsed_time(t_end)
     stage_ms = {st: statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps))
                 for i, st in enumerate(STAGES)}
-    ms = ms_local
-    if world > 1:
-        t = torch.tensor([ms_local], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-        torch.distributed.barrier()
     ms_per_step = ms / args.steps
-    value = world * T * args.steps / (ms / 1e3)
+    value = T * args.steps / (ms / 1e3)
 
-    # end to end through the public call, host buffers, copies inside the
-    # timing: x goes up by a copy from page-locked memory; the result comes
-    # back either written straight into mapped page-locked memory by the
-    # unpermute kernel or (where the host buffer is not mapped) by a copy
+    peaks = load_peaks()
+    dom = max(("gemm_gateup", "gemm_down"), key=lambda s: stage_ms[s])
+    roof = binding_roof(alg[dom + "_bytes"], alg[dom + "_flops"], stage_ms[dom], shape, peaks)
+    roof["kernel"] = dom
+    roof["traffic"] = traffic_for(dom, shape.name)
+    roof["peak_source"] = peaks["source"]
+    layer_roof = binding_roof(alg["layer_bytes"], alg["flops"], ms_per_step, shape, peaks)
+    layer_roof.update({"alg_bytes": alg["layer_bytes"], "alg_flops": alg["flops"],
+                       "tflops": round(alg["flops"] / (ms_per_step / 1e3) / 1e12, 2),
+                       "gbs": round(alg["layer_bytes"] / (ms_per_step / 1e3) / 1e9, 1)})
+    res = {
+        "metric": "routed-MoE layer tokens/s at E=512,k=10,D=4096",
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": {"f32": "f32", "bf16": "bf16", "fp8": "e4m3"}[shape.dtype],
+        "data": "synthetic (seeded; random-init weights of the layer's shape)",
+        "config": {"workload": shape.name, "T": T, "D": shape.D, "E": shape.E, "I": shape.I,
+                   "top_k": shape.top_k, "shared_experts": 1, "router_bias_zipf_s": shape.zipf_s,
+                   "out_dtype": out_dtype(shape), "parallelism": "single GPU",
+                   "l2": "inputs larger than L2 (expert weights stream from HBM every step)",
+                   "touched_experts": alg["touched_experts"]},
+        "roofline": roof,
+        "layer_roofline": layer_roof,
+        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "gpu_launches": int(launches),
+        "clocks": clk.summary(),
+        "impl": "ours",
+        "gemm_path": "tcgen05" if "tcgen05" in L.moe_build_info() else "simt",
+    }
+    if e2e:
+        res["e2e"] = run_e2e(args, layer, x, out, stream)
+    return res, inp, layer
+
+
+def run_e2e(args, layer, x, out, stream):
+    """End to end through the public call, host buffers, copies inside the
+    timing: x goes up by a copy from page-locked memory; the result comes back
+    either written straight into mapped page-locked memory by the unpermute
+    kernel or (where the host buffer is not mapped) by a copy."""
+    T = x.shape[0]
     x_h = x.cpu().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     direct_out = L.moe_pointer_kind(out_h) == "host_mapped"
@@ -255,71 +314,30 @@ def run_ours(args, shape, world, rank, local):
         if i >= args.warmup:
             e2e_ms.append(a.elapsed_time(b))
     layer.check()
-    e2e_ms_step = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([e2e_ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms_step = float(t.item())
+    return {"value": round(T / (statistics.mean(e2e_ms) / 1e3), 1), "unit": "tokens/s",
+            "out_path": "written by the unpermute into mapped page-locked host memory" if direct_out
+            else "device buffer, then a device-to-host copy",
+            "h2d_bytes_per_step": x.numel() * x.element_size(),
+            "d2h_bytes_per_step": out.numel() * out.element_size()}
 
-    peaks = load_peaks()
-    dom = max(("gemm_gateup", "gemm_down"), key=lambda s: stage_ms[s])
-    # the kernel's own roofline: whichever of its algorithmic bytes (at the HBM
-    # copy bandwidth) and flops (at the dense tensor peak of its dtype, the
-    # sustained figure: the kernel runs inside a long step) takes longer
-    tc_peak = (peaks["bf16_tflops_sustained"] or peaks["bf16_tflops"]) * (2.0 if shape.dtype == "fp8" else 1.0)
-    t_hbm = alg[dom + "_bytes"] / (peaks["hbm_gbs"] * 1e9)
-    t_tc = alg[dom + "_flops"] / (tc_peak * 1e12)
-    hbm_bound = shape.dtype == "f32" or t_hbm >= t_tc
-    if hbm_bound:
-        achieved = alg[dom + "_bytes"] / (stage_ms[dom] / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4)}
-    else:
-        achieved = alg[dom + "_flops"] / (stage_ms[dom] / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": tc_peak, "unit": "TFLOP/s",
-                "frac": round(achieved / tc_peak, 4),
-                "peak_note": ("fp8 = 2 x measured bf16 sustained (nominal dense ratio)" if shape.dtype == "fp8"
-                              else "measured bf16 sustained")}
-    roof["kernel"] = dom
-    roof["traffic"] = traffic_for(dom, shape.name)
-    roof["peak_source"] = peaks["source"]
-    layer_gbs = alg["layer_bytes"] / (ms_per_step / 1e3) / 1e9
-    res = {
-        "metric": "routed-MoE layer tokens/s at E=512,k=10,D=4096",
-        "value": round(value, 1),
-        "unit": "tokens/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": {"f32": "f32", "bf16": "bf16", "fp8": "e4m3"}[shape.dtype],
-        "data": "synthetic (seeded; random-init weights of the layer's shape)",
-        "config": {"workload": shape.name, "T": T, "D": shape.D, "E": shape.E, "I": shape.I,
-                   "top_k": shape.top_k, "shared_experts": 1, "router_bias_zipf_s": shape.zipf_s,
-                   "out_dtype": out_dtype(shape),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (expert weights stream from HBM every step)",
-                   "touched_experts": alg["touched_experts"]},
-        "roofline": roof,
-        "layer_roofline": {"bound": "hbm", "achieved": round(layer_gbs, 1), "peak": peaks["hbm_gbs"],
-                           "unit": "GB/s", "frac": round(layer_gbs / peaks["hbm_gbs"], 4),
-                           "alg_bytes": alg["layer_bytes"], "alg_flops": alg["flops"],
-                           "tflops": round(alg["flops"] / (ms_per_step / 1e3) / 1e12, 2)},
-        "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
-        "e2e": {"value": round(world * T / (e2e_ms_step / 1e3), 1), "unit": "tokens/s",
-                "out_path": "written by the unpermute into mapped page-locked host memory" if direct_out
-                else "device buffer, then a device-to-host copy",
-                "h2d_bytes_per_step": x.numel() * x.element_size(),
-                "d2h_bytes_per_step": out.numel() * out.element_size()},
-        "gpu_launches": int(launches),
-        "clocks": clk.summary(),
-        "impl": "ours",
-        "gemm_path": "tcgen05" if "tcgen05" in L.moe_build_info() else "simt",
-    }
-    return res, inp, layer
+
+# The other large workloads, timed in the same process after the headline one
+# (same steps and warm-up; each one's weights freed before the next).
+EXTRA_BENCH = ("BATCHED_DECODE_BF16", "PREFILL_BF16", "PREFILL_FP8")
+EXTRA_KEYS = ("value", "ms_per_step", "roofline", "layer_roofline", "stage_ms", "e2e", "gpu_launches", "clocks",
+              "dtype", "config")
+
+
+def run_extra_workloads(args, local):
+    out = {}
+    for name in EXTRA_BENCH:
+        shape = getattr(synth, name)
+        res, inp, layer = run_ours(args, shape, local)
+        out[shape.name] = {k: res[k] for k in EXTRA_KEYS if k in res}
+        del res, inp, layer
+        torch.cuda.synchronize(local)
+        torch.cuda.empty_cache()
+    return out
 
 
 # ------------------------------------------------------------ oracle leg
@@ -415,6 +433,9 @@ def main():
                     choices=sorted(synth.WORKLOADS) + sorted(synth.EXTRA_WORKLOADS))
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="time only --workload (by default the decode line also times batched decode, "
+                         "prefill bf16 and FP8 prefill under its 'workloads' key)")
     ap.add_argument("--flags", type=int, default=0, help="moe_config.flags (kernel-path overrides)")
     ap.add_argument("--cpu-tokens", type=int, default=128, help="oracle sample size for cpu_baseline")
     ap.add_argument("--experts", type=int, default=0,
@@ -428,19 +449,24 @@ def main():
         import dataclasses
         shape = dataclasses.replace(shape, E=args.experts, name=f"{shape.name}_E{args.experts}_profile")
     world, rank, local = dist_env()
+    if world > 1 and args.impl == "ours":
+        # The layer runs on one GPU and shards nothing; its prefill GEMMs pair
+        # CTAs in 2-CTA clusters that share operand tiles through TMA
+        # multicast, which is kept to single-GPU processes.  So a multi-rank
+        # launch of this arm stops here, before the library is loaded.
+        print(f"bench.py: --impl ours runs on one GPU only (WORLD_SIZE={world}); "
+              "refused before loading libmoe", file=sys.stderr, flush=True)
+        sys.exit(3)
     if world > 1:
-        backend = "nccl" if args.impl == "ours" else "gloo"
-        if args.impl == "ours":
-            torch.cuda.set_device(local)
-        torch.distributed.init_process_group(backend)
+        torch.distributed.init_process_group("gloo")
     try:
         if args.impl == "reference":
             res = run_reference(args, shape, world, rank, local)
             if res is not None:
                 print(json.dumps(res), flush=True)
             return
-        res, inp, layer = run_ours(args, shape, world, rank, local)
-        if rank == 0 and not args.no_cpu_baseline:
+        res, inp, layer = run_ours(args, shape, local)
+        if not args.no_cpu_baseline:
             import oracle
             oracle.build()
             ntok, dt = oracle_sample(shape, inp, args.cpu_tokens)
@@ -449,8 +475,11 @@ def main():
                                    "kind": "oracle",
                                    "sample": f"{ntok} of {shape.T} tokens, whole layer in fp64 "
                                              f"(router, top-k, {shape.top_k} experts + shared), {dt:.1f} s"}
-        if rank == 0:
-            print(json.dumps(res), flush=True)
+        if args.workload == synth.DECODE_BF16.name and not args.experts and not args.no_extra_workloads:
+            del inp, layer
+            torch.cuda.empty_cache()
+            res["workloads"] = run_extra_workloads(args, local)
+        print(json.dumps(res), flush=True)
     finally:
         if world > 1:
             torch.distributed.destroy_process_group()

@@ -75,3 +75,24 @@ def test_clock_summary_keeps_samples_inside_the_timed_window(tmp_path):
     c.t_end = datetime.datetime.strptime(rows[2][0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
     s = c.summary()
     assert s["sm_mhz"] == 2025.0 and s["sm_max_mhz"] == 2070.0 and s["reasons"] == ["sw_power_cap"]
+
+
+def test_our_arm_refuses_more_than_one_rank_before_loading_the_library():
+    """--impl ours is single-GPU: under WORLD_SIZE=2 it exits non-zero with a
+    message, and libmoe is never mapped into the process."""
+    probe = (
+        "import runpy, sys\n"
+        "sys.argv = ['bench.py', '--impl', 'ours', '--steps', '2', '--warmup', '3']\n"
+        "rc = 0\n"
+        "try:\n"
+        "    runpy.run_path('bench.py', run_name='__main__')\n"
+        "except SystemExit as e:\n"
+        "    rc = e.code\n"
+        "maps = open('/proc/self/maps').read()\n"
+        "print('LIBMOE_MAPPED' if 'libmoe' in maps else 'LIBMOE_ABSENT')\n"
+        "sys.exit(rc)\n")
+    env = dict(os.environ, WORLD_SIZE="2", RANK="0", LOCAL_RANK="0", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", probe], capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
+    assert r.returncode != 0
+    assert "one GPU only" in r.stderr and "refused before loading libmoe" in r.stderr
+    assert "LIBMOE_ABSENT" in r.stdout
