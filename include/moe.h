@@ -46,7 +46,10 @@
  *                           fp32 block scales, MOE_FP8_E4M3_B128 only.
  *   w_down_f16 [E+1, D, I]  fp16 copy of w_down (MOE_BF16 layer on tensor
  *                           cores, unless MOE_FLAG_DOWN_HILO); made once by
- *                           moe_convert_down_weights().
+ *                           moe_convert_down_weights().  Where it is read
+ *                           (MOE_BF16 without MOE_FLAG_DOWN_HILO or
+ *                           MOE_FLAG_FORCE_SIMT) w_down itself is not, and
+ *                           may be NULL: the caller can free the bf16 copy.
  * Every matrix is [out_features, in_features]: the reduction dimension is
  * innermost (K-major), which is what the tensor-core operand loads want.
  */
@@ -265,7 +268,9 @@ MOE_API moe_status moe_unpermute(const moe_plan* plan, int32_t T, void* out, voi
  * E <= 1024, 1 <= top_k <= min(E, 32).
  * The first call on a device looks up the array's device address with
  * cudaGetSymbolAddress (with that device current); make that first call
- * before any stream capture.  Every call on a device shares the one array:
+ * before any stream capture.  The address is kept for the life of the
+ * process: after cudaDeviceReset (or anything else that replaces the
+ * device's primary context) this entry point must not be called again.  Every call on a device shares the one array:
  * calls that overlap on the GPU (other streams, other threads) race and must
  * be serialised by the caller.  Out-of-range expert ids are skipped (their
  * pairs get no row); there is no error word.  The array keeps the last

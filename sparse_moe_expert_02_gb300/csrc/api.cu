@@ -6,6 +6,9 @@
 
 #include <algorithm>
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "internal.h"
@@ -13,6 +16,42 @@
 namespace moe {
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+namespace {
+std::mutex g_setup_mu;
+std::map<std::pair<const void*, int>, int> g_smem_set;  // (kernel, device) -> bytes allowed
+std::map<std::pair<const void*, int>, int> g_values;    // (key, device) -> value
+}  // namespace
+
+cudaError_t ensure_smem_attr(const void* func, int bytes) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    int& cur = g_smem_set[{func, dev}];
+    if (cur >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) cur = bytes;
+    return e;
+}
+
+cudaError_t per_device_value(const void* key, const std::function<cudaError_t(int*)>& init, int* value) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    auto it = g_values.find({key, dev});
+    if (it != g_values.end()) {
+        *value = it->second;
+        return cudaSuccess;
+    }
+    int v = 0;
+    e = init(&v);
+    if (e != cudaSuccess) return e;
+    g_values[{key, dev}] = v;
+    *value = v;
+    return cudaSuccess;
+}
 }  // namespace moe
 
 struct moe_plan {
@@ -135,10 +174,15 @@ moe_status check_weights(const moe_plan* p, const moe_weights* w, bool router, b
             return arg_fail(MOE_ERR_INVALID_ARG, "b_router NULL or misaligned");
     }
     if (experts) {
-        if (!ptr_ok(w->w_gate) || !ptr_ok(w->w_up) || !ptr_ok(w->w_down))
+        if (!ptr_ok(w->w_gate) || !ptr_ok(w->w_up))
             return arg_fail(MOE_ERR_INVALID_ARG, "expert weight NULL or misaligned");
-        if (f16_down(p->cfg) && !(p->cfg.flags & MOE_FLAG_FORCE_SIMT) && !ptr_ok(w->w_down_f16))
+        // the bf16 layer's tensor-core down GEMM reads only the fp16 copy, so
+        // there the bf16 w_down may be NULL (its memory freed by the caller)
+        const bool f16_only = f16_down(p->cfg) && !(p->cfg.flags & MOE_FLAG_FORCE_SIMT);
+        if (f16_only && !ptr_ok(w->w_down_f16))
             return arg_fail(MOE_ERR_INVALID_ARG, "w_down_f16 NULL or misaligned (see moe_convert_down_weights)");
+        if (f16_only ? (w->w_down && !aligned(w->w_down, 16)) : !ptr_ok(w->w_down))
+            return arg_fail(MOE_ERR_INVALID_ARG, "w_down NULL or misaligned");
         if (p->cfg.dtype == MOE_FP8_E4M3_B128 && (!ptr_ok(w->s_gate) || !ptr_ok(w->s_up) || !ptr_ok(w->s_down)))
             return arg_fail(MOE_ERR_INVALID_ARG, "FP8 block scales NULL or misaligned");
     }

@@ -459,19 +459,20 @@ template <int EPI>
 cudaError_t launch_one(int grid, const CUtensorMap& ma, const CUtensorMap& msh, const CUtensorMap& mb,
                        const CUtensorMap& mb2, const CUtensorMap& maf, const CUtensorMap& mshf, const Params& p,
                        cudaStream_t stream) {
-    static bool attr = false;
-    if (!attr) {
+    int ready = 0;
+    cudaError_t e = per_device_value((const void*)gemm_fp8_kernel<EPI>, [](int* v) {
         // The warpgroup register split (setmaxnreg) balances only at exactly
         // kRegsLaunch registers per thread; anything else could leave the
         // raising warpgroups waiting for registers that never come free.
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, gemm_fp8_kernel<EPI>);
-        if (e != cudaSuccess) return e;
+        cudaError_t e2 = cudaFuncGetAttributes(&fa, gemm_fp8_kernel<EPI>);
+        if (e2 != cudaSuccess) return e2;
         if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(gemm_fp8_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+        e2 = cudaFuncSetAttribute(gemm_fp8_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e2 == cudaSuccess) *v = 1;
+        return e2;
+    }, &ready);
+    if (e != cudaSuccess) return e;
     gemm_fp8_kernel<EPI><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, maf, mshf, p);
     return cudaGetLastError();
 }

@@ -714,8 +714,10 @@ struct Maps {
 template <int EPI, bool PAIR, bool CL>
 cudaError_t launch_one(int grid, const Maps& m, const Params& p, cudaStream_t stream) {
     auto kern = gemm_tc_kernel<EPI, PAIR, CL>;
-    static int ready = 0;  // 0: attributes not set; else (CL) the most co-resident clusters
-    if (!ready) {
+    // per device: the shared-memory limit raised and (CL) the most
+    // co-resident clusters
+    int ready = 0;
+    cudaError_t e0 = per_device_value((const void*)kern, [&](int* v) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         int n = 1;
@@ -738,8 +740,10 @@ cudaError_t launch_one(int grid, const Maps& m, const Params& p, cudaStream_t st
             if (e != cudaSuccess) return e;
             if (n < 1) return cudaErrorInvalidConfiguration;
         }
-        ready = n;
-    }
+        *v = n;
+        return cudaSuccess;
+    }, &ready);
+    if (e0 != cudaSuccess) return e0;
     if (!CL) {
         kern<<<grid, kThreads, kSmemBytes, stream>>>(m.a, m.a_sh, m.b, m.b2, m.af, m.a_shf, m.ah, m.a_shh, p);
         return cudaGetLastError();

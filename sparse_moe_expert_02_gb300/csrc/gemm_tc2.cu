@@ -358,8 +358,8 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& msh, const CUte
                        const CUtensorMap& maf, const CUtensorMap& mshf, const Params& p, int max_units, int num_sms,
                        cudaStream_t stream) {
     auto kern = gemm_tc2_kernel<EPI, PAIR>;
-    static int max_clusters = 0;
-    if (max_clusters == 0) {
+    int max_clusters = 0;
+    cudaError_t e0 = per_device_value((const void*)kern, [&](int* v) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
         cudaLaunchConfig_t qc = {};
@@ -376,8 +376,10 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& msh, const CUte
         int n = 0;
         e = cudaOccupancyMaxActiveClusters(&n, (void*)kern, &qc);
         if (e != cudaSuccess || n < 1) return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
-        max_clusters = n;
-    }
+        *v = n;
+        return cudaSuccess;
+    }, &max_clusters);
+    if (e0 != cudaSuccess) return e0;
     const int clusters = std::max(1, std::min(max_clusters, max_units));
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters);

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <functional>
+
 #include "moe.h"
 
 namespace moe {
@@ -72,6 +74,17 @@ struct GroupedGemm {
 // Kernel launch accounting (moe_launch_count): every launcher adds the
 // number of kernels it enqueued.
 void count_launches(int n);
+
+// One-time, per-device kernel set-up.  cudaFuncSetAttribute and occupancy
+// queries act on the current device only, so their results are remembered
+// per (key, current device), under a lock (launchers may run on several host
+// threads and devices).
+//   ensure_smem_attr: raise `func`'s dynamic shared-memory limit on the
+//     current device to at least `bytes` (a no-op once it is that high).
+//   per_device_value: `init` runs once per (key, device) with the lock held;
+//     later calls on that device return the value it produced.
+cudaError_t ensure_smem_attr(const void* func, int bytes);
+cudaError_t per_device_value(const void* key, const std::function<cudaError_t(int*)>& init, int* value);
 
 // Launchers (all asynchronous on `stream`; return cudaGetLastError()).
 cudaError_t launch_gemm_simt(const GroupedGemm& g, cudaStream_t stream);

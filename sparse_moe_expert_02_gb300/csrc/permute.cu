@@ -265,13 +265,8 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
                                  uint32_t* err, cudaStream_t stream) {
     const int64_t TK = (int64_t)T * k;
     if (TK <= kSmallPairs && E <= kSmallMaxE) {
-        static bool attr = false;
-        if (!attr) {
-            cudaError_t e = cudaFuncSetAttribute(perm_index_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 kSmallSmem);
-            if (e != cudaSuccess) return e;
-            attr = true;
-        }
+        cudaError_t e = ensure_smem_attr((const void*)perm_index_small_kernel, kSmallSmem);
+        if (e != cudaSuccess) return e;
         const int smem = (32 * E + 4 * (E + 2)) * 4;
         perm_index_small_kernel<<<1, 1024, smem, stream>>>(idx, T, E, k, counts, offsets, tiles, tiles2, inv, src_tok,
                                                            err);
@@ -281,12 +276,10 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
     const int nch = (int)cdiv(TK, perm_chunk(TK));
     perm_hist_kernel<<<nch, 256, E * sizeof(int32_t), stream>>>(idx, TK, E, hist, err);
     perm_scan_kernel<<<1, 1024, 0, stream>>>(hist, nch, E, T, counts, offsets, tiles, tiles2, src_tok, TK);
-    static int rank_smem_set = 0;
     const int rank_smem = kRankWarps * E * (int)sizeof(int32_t);
-    if (rank_smem > 48 * 1024 && rank_smem_set < rank_smem) {
-        cudaError_t e = cudaFuncSetAttribute(perm_rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, rank_smem);
+    if (rank_smem > 48 * 1024) {
+        cudaError_t e = ensure_smem_attr((const void*)perm_rank_kernel, rank_smem);
         if (e != cudaSuccess) return e;
-        rank_smem_set = rank_smem;
     }
     perm_rank_kernel<<<nch, 32 * kRankWarps, rank_smem, stream>>>(idx, TK, k, E, hist, offsets, inv, src_tok);
     count_launches(3);

@@ -40,13 +40,13 @@ class MoELayer:
                     w[n + "_f32"] = src
         else:
             for n in ("w_gate", "w_up", "w_down"):
-                w[n] = weights[n]
+                w[n] = weights.get(n)
         self.ws = torch.empty(L.moe_workspace_size(self.plan, T_max), dtype=torch.uint8, device=dev)
         L.moe_workspace_init(self.plan, self.ws)
         self.hilo = dtype == "bf16" and bool(flags & L.MOE_FLAG_DOWN_HILO)
-        if dtype == "bf16" and not self.hilo and w.get("w_down") is not None:
+        if dtype == "bf16" and not self.hilo:
             if weights.get("w_down_f16") is not None:
-                w["w_down_f16"] = weights["w_down_f16"]
+                w["w_down_f16"] = weights["w_down_f16"]  # w_down may then be absent
             else:
                 wd = w["w_down"].contiguous()
                 w["w_down"] = wd

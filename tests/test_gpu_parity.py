@@ -507,3 +507,41 @@ def test_full_size_fp8_decode(shape):
     layer, out, err = _layer_parity(shape, inp, rows=rows, out_dtype="bf16", check_y=False)
     del layer, inp
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------ boundary: w_down optional
+
+def test_bf16_tensor_core_layer_runs_without_the_bf16_w_down():
+    """Where the down GEMM reads the fp16 copy, the bf16 w_down may be NULL
+    (the caller frees it): the output is the same, bit for bit."""
+    shape = synth.SMALL_BF16
+    inp = _dev_inputs(shape, seed=7)
+    full = MoELayer.from_shape(shape, inp)
+    ref = full.forward(inp["x"])
+    inp2 = {n: t for n, t in inp.items() if n != "w_down"}
+    inp2["w_down_f16"] = full.w["w_down_f16"]
+    lean = MoELayer.from_shape(shape, inp2)
+    assert lean.w["w_down"] is None
+    out = lean.forward(inp["x"])
+    lean.check()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
+@pytest.mark.parametrize("flags", [L.MOE_FLAG_FORCE_SIMT, L.MOE_FLAG_DOWN_HILO], ids=["simt", "hilo"])
+def test_null_bf16_w_down_is_refused_where_it_is_read(flags):
+    """The CUDA-core and hi/lo down GEMMs read the bf16 w_down: NULL there is
+    an argument error, returned before anything is launched."""
+    shape = synth.SMALL_BF16
+    inp = _dev_inputs(shape, seed=7)
+    layer = MoELayer.from_shape(shape, inp, flags=flags)
+    w = dict(layer.w)
+    w["w_down"] = None
+    cw = L.make_weights(w)
+    out = layer.new_out(shape.T)
+    torch.cuda.synchronize()
+    l0 = L.moe_launch_count()
+    with pytest.raises(L.MoEError) as ei:
+        L.moe_forward(layer.plan, cw, inp["x"], shape.T, out, None, None, layer.ws)
+    assert ei.value.status == L.MOE_ERR_INVALID_ARG
+    assert L.moe_launch_count() == l0

@@ -43,18 +43,22 @@ def _noalloc(idx, T, E, k):
 
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_path_two_calls_in_a_row():
-    # a large skewed problem first (many chunks), then a small one: the second
-    # call runs over the array as the first one left it
-    cases = [(synth.PREFILL_BF16, 1), (synth.SMALL_BF16, 2)]
+    # Calls in a row on one array: a large skewed problem (80 chunks of 1024
+    # pairs x 512 experts of histograms), then a smaller chunked one (20
+    # chunks x 64 experts) whose scan runs over the entries the first call
+    # left behind, then one small enough for the single-block kernel.
+    cases = [
+        (synth.LayerShape("noalloc_T8192_E512_k10", 8192, 128, 512, 128, 10, "bf16", 1.2), 1),
+        (synth.LayerShape("noalloc_T2000_E64_k10", 2000, 128, 64, 128, 10, "bf16", 1.0), 2),
+        (synth.LayerShape("noalloc_T300_E32_k4", 300, 128, 32, 128, 4, "bf16", 1.2), 3),
+    ]
     for shape, seed in cases:
-        small = synth.LayerShape(shape.name, shape.T, 128 if shape.D > 512 else shape.D, shape.E,
-                                 128, shape.top_k, "bf16", shape.zipf_s)
-        layer, v = _workspace_reference(small, seed)
-        T, E, k = small.T, small.E, small.top_k
+        layer, v = _workspace_reference(shape, seed)
+        T, E, k = shape.T, shape.E, shape.top_k
         out = _noalloc(v["blob"][0], T, E, k)
         torch.cuda.synchronize()
         for name in ("counts", "offsets", "tiles", "inv", "src_tok"):
-            assert torch.equal(out[name], v[name]), name
+            assert torch.equal(out[name], v[name]), (shape.name, name)
         layer.check()
 
 
