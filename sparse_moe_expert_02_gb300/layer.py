@@ -47,7 +47,7 @@ class MoELayer:
         if dtype == "bf16" and not self.hilo:
             if weights.get("w_down_f16") is not None:
                 w["w_down_f16"] = weights["w_down_f16"]  # w_down may then be absent
-            else:
+            elif w.get("w_down") is not None:
                 wd = w["w_down"].contiguous()
                 w["w_down"] = wd
                 w["w_down_f16"] = torch.empty(wd.shape, dtype=torch.float16, device=dev)
