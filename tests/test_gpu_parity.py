@@ -11,7 +11,8 @@ import pytest
 import torch
 
 import oracle
-from parity_util import err_quantiles, experts_for_tokens, rel_max_err, sample_rows
+from parity_util import (err_quantiles, experts_for_tokens, full_size_rows, rel_max_err, sample_rows,
+                         y_reference)
 from sparse_moe_expert_02_gb300 import MoELayer, synth
 from sparse_moe_expert_02_gb300 import _lib as L
 
@@ -464,8 +465,54 @@ def test_fp8_h_codes_mostly_match_oracle():
 @pytest.fixture(scope="module")
 def big_bf16_weights():
     w = synth.make_inputs(synth.DECODE_BF16, seed=0, device="cuda", T=1)
-    yield {n: w[n] for n in ("w_gate", "w_up", "w_down")}
+    w = {n: w[n] for n in ("w_gate", "w_up", "w_down")}
+    host = {n: t.cpu() for n, t in w.items()}   # the oracle reads expert subsets from here
+    yield w, host
     torch.cuda.empty_cache()
+
+
+def _full_size_parity(shape, inp, host_weights=None, flags=0, out_dtype="f32"):
+    """Full-size workload: routing and permutation bit-exact for all tokens;
+    expert outputs y element-wise on the rows where the tiling changes (the
+    first and last row of every touched group, the 128-row tile boundaries of
+    the five largest groups, every row of the largest group, the shared
+    group's ends); the layer output on 64 sampled tokens plus the tokens of
+    the largest group."""
+    T, E, k = shape.T, shape.E, shape.top_k
+    tol = TOL[shape.dtype]
+    layer = MoELayer.from_shape(shape, inp, flags=flags, out_dtype=out_dtype)
+    x = inp["x"]
+    out = layer.forward(x)
+    layer.check()
+    torch.cuda.synchronize()
+    idx, w, inv, src = _routing_parity(layer, T, E, k)
+    v = layer.views(T)
+    counts = v["counts"].cpu().numpy()
+    offsets = v["offsets"].cpu().numpy()
+    y_rows, e0 = full_size_rows(counts, offsets, T, k)
+    wsrc = host_weights if host_weights is not None else inp
+    ref = y_reference(y_rows, src, offsets, T, k, x, wsrc, shape.dtype, E)
+    y = v["y"][torch.as_tensor(y_rows, device="cuda")].double().cpu().numpy()
+    worst = 0.0
+    for i, r in enumerate(y_rows):
+        e = rel_max_err(y[i], ref[int(r)])
+        worst = max(worst, e)
+        assert e <= 2 * tol, f"y row {r}: max|err|/rms {e:.3e}"
+    # out: sampled tokens plus (a subsample of) the largest group's tokens
+    g = np.random.default_rng(7)
+    toks = src[offsets[e0]:offsets[e0] + counts[e0]]
+    if len(toks) > 256:
+        toks = np.sort(g.choice(toks, 256, replace=False))
+    rows = np.union1d(sample_rows(T, 64, seed=1), toks)
+    ex, idx_sub = experts_for_tokens(idx[rows], wsrc, shape.dtype, E)
+    ref_out = oracle.moe_tokens(x[torch.as_tensor(rows, device=x.device)].cpu(), idx_sub, w[rows], ex)
+    got = out[torch.as_tensor(rows, device="cuda")].double().cpu().numpy()
+    err = rel_max_err(got, ref_out)
+    print(f"{shape.name} flags={flags:#x}: {len(y_rows)} y rows worst {worst:.3e}; {len(rows)} out rows "
+          f"max|err|/rms {err:.3e}")
+    assert err <= tol
+    assert torch.isfinite(out).all()
+    return layer, counts
 
 
 @pytest.mark.parametrize("shape,flags", [(synth.DECODE_BF16, 0), (synth.BATCHED_DECODE_BF16, 0),
@@ -473,28 +520,26 @@ def big_bf16_weights():
                                          (synth.PREFILL_BF16, L.MOE_FLAG_MCAST_OFF),
                                          (synth.BATCHED_DECODE_BF16, L.MOE_FLAG_MCAST_ON),
                                          (synth.PREFILL_BF16, L.MOE_FLAG_NARROW_TAILS_OFF),
+                                         (synth.PREFILL_BF16, L.MOE_FLAG_NARROW_TAILS_OFF | L.MOE_FLAG_MCAST_OFF),
                                          (synth.DECODE_BF16, L.MOE_FLAG_NARROW_TAILS_ON)],
                          ids=["decode", "batched_decode", "prefill", "prefill_cta_pairs", "prefill_no_tile_pairs",
-                              "batched_decode_tile_pairs", "prefill_wide_tails", "decode_narrow_tails"])
+                              "batched_decode_tile_pairs", "prefill_wide_tails", "prefill_plain",
+                              "decode_narrow_tails"])
 def test_full_size_bf16_workloads(shape, flags, big_bf16_weights):
+    w_dev, w_host = big_bf16_weights
     inp = _dev_inputs(shape, seed=0, weights=False)
-    inp.update(big_bf16_weights)
-    rows = sample_rows(shape.T, 6, seed=1)
-    layer, out, _ = _layer_parity(shape, inp, rows=rows, check_y=False, flags=flags)
+    inp.update(w_dev)
+    layer, counts = _full_size_parity(shape, inp, host_weights=w_host, flags=flags)
     if shape.zipf_s is not None and shape.T >= 8192:
-        counts = layer.views(shape.T)["counts"][:shape.E].cpu().numpy()
         mean = shape.T * shape.top_k / shape.E
-        assert counts.max() > 10 * mean, "the skewed workload must have straggler experts"
-    assert torch.isfinite(out).all()
+        assert counts[:shape.E].max() > 10 * mean, "the skewed workload must have straggler experts"
 
 
 def test_full_size_fp8_prefill():
     shape = synth.PREFILL_FP8
     inp = _dev_inputs(shape, seed=0)
-    rows = sample_rows(shape.T, 4, seed=2)
-    layer, out, err = _layer_parity(shape, inp, rows=rows, out_dtype="bf16", check_y=False)
-    counts = layer.views(shape.T)["counts"][:shape.E].cpu().numpy()
-    assert counts.max() > 10 * shape.T * shape.top_k / shape.E
+    layer, counts = _full_size_parity(shape, inp, out_dtype="bf16")
+    assert counts[:shape.E].max() > 10 * shape.T * shape.top_k / shape.E
     del layer, inp
     torch.cuda.empty_cache()
 
@@ -503,8 +548,7 @@ def test_full_size_fp8_prefill():
 def test_full_size_fp8_decode(shape):
     """FP8 weights at the decode shapes (half the streamed bytes)."""
     inp = _dev_inputs(shape, seed=0)
-    rows = sample_rows(shape.T, 4, seed=3)
-    layer, out, err = _layer_parity(shape, inp, rows=rows, out_dtype="bf16", check_y=False)
+    layer, _ = _full_size_parity(shape, inp, out_dtype="bf16")
     del layer, inp
     torch.cuda.empty_cache()
 
