@@ -124,6 +124,13 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2 } moe_
  * than the MMA time saved. */
 #define MOE_FLAG_NARROW_TAILS_ON 0x40u   /* narrow tails in both expert GEMMs at every size */
 #define MOE_FLAG_NARROW_TAILS_OFF 0x80u  /* every tile as 128 rows x N features */
+/* Top-k + histogram: where the permutation works in chunks (more than 16384
+ * (token, slot) pairs, or E > 512), moe_forward's top-k kernel also counts
+ * the chosen experts into the permutation's per-chunk histograms, and the
+ * permutation skips its own pass over the indices (English page, "The
+ * Remaining Roadmap": fusing the top-k selection).  Results are identical
+ * either way; this flag turns the fusion off. */
+#define MOE_FLAG_TOPK_HIST_OFF 0x100u
 
 typedef struct moe_config {
     int32_t T_max;           /* largest token count a call may pass */

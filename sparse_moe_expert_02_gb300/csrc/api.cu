@@ -371,6 +371,14 @@ moe_status moe_topk(const moe_plan* p, int32_t T, void* ws, size_t ws_bytes, voi
     return MOE_OK;
 }
 
+namespace {
+// moe_forward's route: with fused_hist the top-k kernel also counts the
+// permutation's per-chunk expert histograms (zeroed here first), so that the
+// permutation skips its own histogram pass.
+moe_status route_impl(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, Ws& W, void* stream,
+                      bool fused_hist);
+}  // namespace
+
 moe_status moe_route(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, void* ws, size_t ws_bytes,
                      void* stream) {
     Ws W;
@@ -378,6 +386,26 @@ moe_status moe_route(const moe_plan* p, const moe_weights* w, const void* x, int
     if (st != MOE_OK) return st;
     if ((st = check_weights(p, w, true, false)) != MOE_OK) return st;
     if (!ptr_ok(x)) return arg_fail(MOE_ERR_INVALID_ARG, "x NULL or misaligned");
+    return route_impl(p, w, x, T, W, stream, false);
+}
+
+namespace {
+bool fuse_topk_hist(const moe_plan* p, int32_t T) {
+    return !(p->cfg.flags & MOE_FLAG_TOPK_HIST_OFF) && moe::permute_uses_chunks((int64_t)T * p->cfg.top_k, p->cfg.E);
+}
+
+// Zero the per-chunk histograms the fused top-k counts into.  moe_forward
+// does this before it forks the shared-expert stream, so that the router
+// GEMM is still the first kernel queued after the fork (a memset there let
+// the shared GEMMs take the SMs first: 2.30 vs 2.25 ms at T=8192).
+cudaError_t zero_topk_hist(const moe_plan* p, int32_t T, Ws& W, cudaStream_t s) {
+    const int64_t TK = (int64_t)T * p->cfg.top_k;
+    return cudaMemsetAsync(W.at<int32_t>(W.L.hist), 0, (size_t)moe::cdiv(TK, moe::perm_chunk(TK)) * p->cfg.E * 4, s);
+}
+
+moe_status route_impl(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, Ws& W, void* stream,
+                      bool fused_hist) {
+    moe_status st;
     const moe_config& c = p->cfg;
     moe::GroupedGemm g = {};
     g.G = 1;
@@ -406,18 +434,24 @@ moe_status moe_route(const moe_plan* p, const moe_weights* w, const void* x, int
         g.out = W.at<float>(W.L.logits_part);
         g.bias = nullptr;
     }
+    int32_t* hist = nullptr;
+    int chunk = 1;
+    if (fused_hist) {  // the caller zeroed the histograms (zero_topk_hist)
+        chunk = moe::perm_chunk((int64_t)T * c.top_k);
+        hist = W.at<int32_t>(W.L.hist);
+    }
     if ((st = run_gemm(p, g, (cudaStream_t)stream, "router GEMM")) != MOE_OK) return st;
     if (S > 1)
         MOE_CUDA(moe::launch_topk(W.at<float>(W.L.logits_part), S, c.has_router_bias ? w->b_router : nullptr,
                                   W.at<float>(W.L.logits), T, c.E, c.top_k, W.at<int32_t>(W.L.blob),
-                                  W.at<uint32_t>(W.L.err), (cudaStream_t)stream));
+                                  W.at<uint32_t>(W.L.err), (cudaStream_t)stream, hist, chunk));
     else
         MOE_CUDA(moe::launch_topk(W.at<float>(W.L.logits), 1, nullptr, nullptr, T, c.E, c.top_k,
-                                  W.at<int32_t>(W.L.blob), W.at<uint32_t>(W.L.err), (cudaStream_t)stream));
+                                  W.at<int32_t>(W.L.blob), W.at<uint32_t>(W.L.err), (cudaStream_t)stream, hist,
+                                  chunk));
     return MOE_OK;
 }
 
-namespace {
 // Permuted copy of x: from T >= 1024 tokens one warp per token reads its row
 // once and writes its top_k copies (x leaves DRAM once); below that there
 // are too few tokens to fill the GPU and one warp per output row gathers.
@@ -425,14 +459,16 @@ bool scatter_by_token(int32_t T) { return T >= 1024; }
 
 // quant_x: the FP8 layer quantises x into xq here (false when the caller
 // already did).
-moe_status permute_impl(const moe_plan* p, const void* x, int32_t T, Ws& W, cudaStream_t s, bool quant_x) {
+// hist_ready: route_impl already counted the per-chunk histograms.
+moe_status permute_impl(const moe_plan* p, const void* x, int32_t T, Ws& W, cudaStream_t s, bool quant_x,
+                        bool hist_ready = false) {
     const moe_config& c = p->cfg;
     const int TK = T * c.top_k;
     MOE_CUDA(moe::launch_permute_index(W.at<int32_t>(W.L.blob), T, c.E, c.top_k, W.at<int32_t>(W.L.hist),
                                        W.at<int32_t>(W.L.counts), W.at<int32_t>(W.L.offsets),
                                        W.at<int32_t>(W.L.tiles), W.at<int32_t>(W.L.tiles2), W.at<int32_t>(W.L.inv),
                                        W.at<int32_t>(W.L.src_tok),
-                                       W.at<uint32_t>(W.L.err), s));
+                                       W.at<uint32_t>(W.L.err), s, hist_ready));
     if (c.dtype == MOE_FP8_E4M3_B128) {
         if (quant_x)
             MOE_CUDA(moe::launch_quant_rows(x, moe::kBF16, T, c.D, W.at<uint8_t>(W.L.xq), W.at<float>(W.L.xq_scale), s));
@@ -631,6 +667,8 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
     cudaStream_t s = (cudaStream_t)stream;
     const moe_config& cf = p->cfg;
     MOE_CUDA(cudaMemsetAsync(ws, 0, kErrBlock, s));
+    const bool fh = fuse_topk_hist(p, T);
+    if (fh) MOE_CUDA(zero_topk_hist(p, T, W, s));
     moe::GroupedGemm gu = gateup_gemm(p, w, x, T, W), dn = down_gemm(p, w, T, W);
     const bool fp8 = cf.dtype == MOE_FP8_E4M3_B128;
     moe::GroupedGemm sgu = shared_only(gu, cf, T, true, fp8 ? (const void*)W.at<uint8_t>(W.L.xq) : x,
@@ -660,20 +698,20 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
         // the router GEMM is enqueued first so that it gets the SMs; the
         // shared GEMMs fill them as its CTAs retire and run beside the
         // top-k and permutation kernels
-        st = moe_route(p, w, x, T, ws, ws_bytes, stream);
+        st = route_impl(p, w, x, T, W, stream, fh);
         MOE_CUDA(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
         moe_status side_st = run_gemm(p, sgu, p->side, "shared gate/up GEMM");
         if (side_st == MOE_OK) side_st = run_gemm(p, sdn, p->side, "shared down GEMM");
         MOE_CUDA(cudaEventRecord(p->ev_join, p->side));
-        if (st == MOE_OK) st = permute_impl(p, x, T, W, s, !fp8);
+        if (st == MOE_OK) st = permute_impl(p, x, T, W, s, !fp8, fh);
         if (st == MOE_OK) st = run_gemm(p, gu, s, "gate/up GEMM");
         if (st == MOE_OK) st = run_gemm(p, dn, s, "down GEMM");
         MOE_CUDA(cudaStreamWaitEvent(s, p->ev_join, 0));  // joined even after an error (stream capture)
         if (side_st != MOE_OK) return side_st;
         if (st != MOE_OK) return st;
     } else {
-        if ((st = moe_route(p, w, x, T, ws, ws_bytes, stream)) != MOE_OK) return st;
-        if ((st = moe_permute(p, x, T, ws, ws_bytes, stream)) != MOE_OK) return st;
+        if ((st = route_impl(p, w, x, T, W, stream, fh)) != MOE_OK) return st;
+        if ((st = permute_impl(p, x, T, W, s, true, fh)) != MOE_OK) return st;
         if ((st = run_gemm(p, gu, s, "gate/up GEMM")) != MOE_OK) return st;
         if ((st = run_gemm(p, dn, s, "down GEMM")) != MOE_OK) return st;
     }

@@ -60,9 +60,11 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t q) {
     return __half2float(__half(hr));
 }
 
-// SiLU(a) * u in fp32: a / (1 + e^-a) * u (the hardware exponential: its
-// few-ulp error is far below what the layer's outputs are compared at).
-__device__ __forceinline__ float swiglu(float a, float u) { return a / (1.0f + __expf(-a)) * u; }
+// SiLU(a) * u in fp32: a * u / (1 + e^-a), with the hardware exponential
+// and the fast (reciprocal-based) division: a few ulp of fp32, far below the
+// fp16 / E4M3 rounding of h that follows.  For a < -88, e^-a is infinite
+// and the quotient is 0, SiLU's limit.
+__device__ __forceinline__ float swiglu(float a, float u) { return __fdividef(a * u, 1.0f + __expf(-a)); }
 
 __host__ __device__ constexpr int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 

@@ -56,7 +56,10 @@ static_assert(kThreads * kRegsLaunch <= 65536, "launch registers exceed the SM")
 constexpr int kAccCols = 256;
 constexpr int kBoxRowsA = 16;
 constexpr uint32_t kBarBytes = 512;  // mbarriers, TMEM address, abort flag, unit ring
-constexpr uint32_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + kBarBytes + 2 * 2 * 128 * 4;
+// Shared copies of the row-tile prefix and the row offsets (G <= 1025
+// groups): the producer finds a unit's group without leaving the SM.
+constexpr int kTabEntries = 1056;
+constexpr uint32_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + kBarBytes + 2 * 2 * 128 * 4 + 2 * kTabEntries * 4;
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_PLAIN = 1 };
 
@@ -85,15 +88,16 @@ struct Unit {
     int g, m0, row0, nrows, nb;
 };
 
-__device__ __forceinline__ Unit decode_unit(const Params& p, int u) {
+// s_tiles / s_off: shared copies of p.tiles and p.offsets (entries 0..G).
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u, const int32_t* s_tiles, const int32_t* s_off) {
     Unit r;
     const int rt = u / p.NB;
     r.nb = u - rt * p.NB;
     if (p.offsets) {
-        r.g = find_group(p.tiles, p.G, rt);
-        r.m0 = (rt - __ldg(p.tiles + r.g)) * BM;
-        r.row0 = __ldg(p.offsets + r.g);
-        r.nrows = __ldg(p.offsets + r.g + 1) - r.row0;
+        r.g = find_group_smem(s_tiles, p.G, rt);
+        r.m0 = (rt - s_tiles[r.g]) * BM;
+        r.row0 = s_off[r.g];
+        r.nrows = s_off[r.g + 1] - r.row0;
     } else {
         r.g = 0;
         r.m0 = rt * BM;
@@ -124,9 +128,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t ufull0 = smem_u32(bars + 2 * kStages + 13), uempty0 = smem_u32(bars + 2 * kStages + 17);
     uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kStages + 21);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+    // unit ring slots: [4][6] = unit number, then its decoded group, m0, row0,
+    // nrows, nb (the producer decodes each unit once for every role)
     volatile int* s_units = (volatile int*)(tmem_slot + 2);
-    static_assert((2 * kStages + 21) * 8 + 6 * 4 <= kBarBytes, "barrier block overflows");
+    static_assert((2 * kStages + 21) * 8 + 8 + 4 * 6 * 4 <= kBarBytes, "barrier block overflows");
     float* s_amax = (float*)(smem + kStages * (kABytes + kBBytes) + kBarBytes);  // [2 units][2 halves][128 rows]
+    int32_t* s_tiles = (int32_t*)(s_amax + 2 * 2 * 128);
+    int32_t* s_off = s_tiles + kTabEntries;
+    if (p.offsets)
+        for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
+            s_tiles[i] = __ldg(p.tiles + i);
+            s_off[i] = __ldg(p.offsets + i);
+        }
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -183,10 +196,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                s_units[i & 3] = u;
+                Unit un = {};
+                if (u >= 0) un = decode_unit(p, u, s_tiles, s_off);
+                volatile int* slot = s_units + 6 * (i & 3);
+                slot[0] = u;
+                slot[1] = un.g;
+                slot[2] = un.m0;
+                slot[3] = un.row0;
+                slot[4] = un.nrows;
+                slot[5] = un.nb;
                 mbar_arrive(ufull0 + 8 * (i & 3));
                 if (u < 0) break;
-                const Unit un = decode_unit(p, u);
                 const bool sh = un.g == p.shared_group;
                 const CUtensorMap* ta = sh ? &tm_a_sh : &tm_a;
                 const CUtensorMap* taf = sh ? &tm_a_shf : &tm_af;
@@ -243,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *abort_flag = 1;
                     break;
                 }
-                const int u = s_units[i & 3];
+                const int u = s_units[6 * (i & 3)];
                 mbar_arrive(uempty0 + 8 * (i & 3));
                 if (u < 0) break;
                 for (int kb = 0; kb < p.KB; ++kb) {
@@ -287,9 +307,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int i = 0; ok; ++i) {
             int u = -1;  // -1: no more units (or a wait that ran out)
+            Unit un = {};
             if (lane == 0) {
                 if (mbar_wait(ufull0 + 8 * (i & 3), (i >> 2) & 1, lim, abort_flag)) {
-                    u = s_units[i & 3];
+                    const volatile int* slot = s_units + 6 * (i & 3);
+                    u = slot[0];
+                    un.g = slot[1];
+                    un.m0 = slot[2];
+                    un.row0 = slot[3];
+                    un.nrows = slot[4];
+                    un.nb = slot[5];
                     mbar_arrive(uempty0 + 8 * (i & 3));
                 } else {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 17, blockIdx.x, i);
@@ -298,8 +325,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             u = __shfl_sync(0xffffffffu, u, 0);
             if (u < 0) break;
+            un.g = __shfl_sync(0xffffffffu, un.g, 0);
+            un.m0 = __shfl_sync(0xffffffffu, un.m0, 0);
+            un.row0 = __shfl_sync(0xffffffffu, un.row0, 0);
+            un.nrows = __shfl_sync(0xffffffffu, un.nrows, 0);
+            un.nb = __shfl_sync(0xffffffffu, un.nb, 0);
             const int unit_par = i & 1;
-            const Unit un = decode_unit(p, u);
             const bool sh = un.g == p.shared_group;
             const int m = un.m0 + row;
             const bool valid = m < un.nrows;
@@ -345,7 +376,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t tb = tmem_base + ((uint32_t)(sub * 32) << 16) + buf * kAccCols;
                 const float f1 = sa * s1, f2 = sa * s2;
                 // Two 32-column TMEM loads per wait, then the promotion with
-                // paired fp32 FMAs (two lanes of work per instruction).
+                // paired fp32 FMAs (two lanes of work per instruction).  The
+                // buffer goes back to the MMA as soon as the second half is
+                // in registers, before that half is promoted: the MMA can
+                // then start the slice after next about 130 cycles sooner.
                 // SwiGLU: q=0 -> gate columns 64*half.., q=1 -> up columns
                 // 128+64*half..; plain: q -> columns 128*half + 64*q.
 #pragma unroll
@@ -354,6 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int col = (EPI == EPI_SWIGLU) ? (q == 0 ? 64 * half : 128 + 64 * half) : 128 * half + 64 * q;
                     tmem_ld32x2(tb + col, r);
                     tmem_wait_ld();
+                    if (q == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(cempty0 + 8 * buf);
+                    }
                     const float f = (EPI == EPI_SWIGLU && q == 1) ? f2 : f1;
                     const float2 ff = make_float2(f, f);
 #pragma unroll
@@ -364,9 +403,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         acc[64 * q + i + 1] = a.y;
                     }
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(cempty0 + 8 * buf);
                 ++chunk;
             }
             if (!ok) break;
@@ -484,6 +520,7 @@ bool gemm_fp8_supported(const GroupedGemm& g) {
     using namespace tc::f8;
     if (g.elem != kE4M3 || !tc::encode_fn()) return false;
     if (!g.offsets && (g.rows < 1 || g.a_shared)) return false;  // single group: A only
+    if (g.offsets && g.G + 1 > kTabEntries) return false;
     if (g.Ka != g.Kb || g.Kb % BKB || g.N % 128) return false;
     if (!g.a_scale || !g.b_scale) return false;
     if (g.b2) {

@@ -97,16 +97,24 @@ bool gemm_fp8_supported(const GroupedGemm& g);
 
 // Top-k over logits = sum_{s<S} part[s] (+ bias), summed in slice order;
 // when S > 1 or bias is given the summed logits are written to logits_out.
+// hist (nullable): also count the chosen experts into the permutation's
+// per-chunk histograms ([chunks][E] with `chunk` pairs per chunk; the caller
+// zeroes them first), which launch_permute_index then takes as given.
 cudaError_t launch_topk(const float* part, int S, const float* bias, float* logits_out, int T, int E, int k,
-                        int32_t* blob, uint32_t* err, cudaStream_t stream);
+                        int32_t* blob, uint32_t* err, cudaStream_t stream, int32_t* hist = nullptr, int chunk = 1);
 int router_splits(int T, int E, int D, int num_sms);
 cudaError_t launch_pack_words(const int32_t* blob, int64_t TK, int32_t* words, cudaStream_t stream);
 
 // tiles2 (nullable): exclusive prefix of ceil(counts/256), the row-tile
 // pairs of the two-CTA GEMM.
+// hist_ready: the per-chunk histograms were already counted (by the top-k
+// kernel) -- only meaningful where permute_uses_chunks().
 cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_t* hist, int32_t* counts,
                                  int32_t* offsets, int32_t* tiles, int32_t* tiles2, int32_t* inv, int32_t* src_tok,
-                                 uint32_t* err, cudaStream_t stream);
+                                 uint32_t* err, cudaStream_t stream, bool hist_ready = false);
+// Whether T*k pairs over E experts take the chunked permutation (per-chunk
+// histograms in the workspace) rather than the single-block one.
+bool permute_uses_chunks(int64_t TK, int E);
 cudaError_t launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t* inv, int T, int k, void* xp,
                                 cudaStream_t stream);
 cudaError_t launch_gather_rows(const void* x, int elem_bytes, int64_t row_bytes, const int32_t* src_tok,

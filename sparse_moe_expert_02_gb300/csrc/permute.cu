@@ -260,11 +260,13 @@ __global__ void __launch_bounds__(1024) perm_index_small_kernel(const int32_t* _
     }
 }
 
+bool permute_uses_chunks(int64_t TK, int E) { return !(TK <= kSmallPairs && E <= kSmallMaxE); }
+
 cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_t* hist, int32_t* counts,
                                  int32_t* offsets, int32_t* tiles, int32_t* tiles2, int32_t* inv, int32_t* src_tok,
-                                 uint32_t* err, cudaStream_t stream) {
+                                 uint32_t* err, cudaStream_t stream, bool hist_ready) {
     const int64_t TK = (int64_t)T * k;
-    if (TK <= kSmallPairs && E <= kSmallMaxE) {
+    if (!permute_uses_chunks(TK, E)) {
         cudaError_t e = ensure_smem_attr((const void*)perm_index_small_kernel, kSmallSmem);
         if (e != cudaSuccess) return e;
         const int smem = (32 * E + 4 * (E + 2)) * 4;
@@ -274,7 +276,7 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
         return cudaGetLastError();
     }
     const int nch = (int)cdiv(TK, perm_chunk(TK));
-    perm_hist_kernel<<<nch, 256, E * sizeof(int32_t), stream>>>(idx, TK, E, hist, err);
+    if (!hist_ready) perm_hist_kernel<<<nch, 256, E * sizeof(int32_t), stream>>>(idx, TK, E, hist, err);
     perm_scan_kernel<<<1, 1024, 0, stream>>>(hist, nch, E, T, counts, offsets, tiles, tiles2, src_tok, TK);
     const int rank_smem = kRankWarps * E * (int)sizeof(int32_t);
     if (rank_smem > 48 * 1024) {
@@ -282,7 +284,7 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
         if (e != cudaSuccess) return e;
     }
     perm_rank_kernel<<<nch, 32 * kRankWarps, rank_smem, stream>>>(idx, TK, k, E, hist, offsets, inv, src_tok);
-    count_launches(3);
+    count_launches(hist_ready ? 2 : 3);
     return cudaGetLastError();
 }
 

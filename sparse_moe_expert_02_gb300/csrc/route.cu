@@ -32,10 +32,15 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 
 // J = ceil(E / 32) logits per lane (a power of two); SB = K slices loaded per
 // batch (1 when the router GEMM did not split K: fewer registers, more warps)
+// hist (nullable): the permutation's per-chunk expert histograms
+// ([chunks][E], zeroed by the caller; chunk = pairs per chunk), counted here
+// as the experts are chosen, so that the permutation needs no pass of its
+// own over the indices.
 template <int J, int SB>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ part, int S,
                                                    const float* __restrict__ bias, float* __restrict__ logits_out,
-                                                   int T, int E, int k, int32_t* __restrict__ blob, uint32_t* err) {
+                                                   int T, int E, int k, int32_t* __restrict__ blob,
+                                                   int32_t* __restrict__ hist, int chunk, uint32_t* err) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;  // whole warps leave together
@@ -156,21 +161,25 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
     if (lane < k) {
         const int64_t TK = (int64_t)T * k;
-        blob[(int64_t)t * k + lane] = isel;
-        blob[TK + (int64_t)t * k + lane] = __float_as_int(ex / sum);
+        const int64_t a = (int64_t)t * k + lane;
+        blob[a] = isel;
+        blob[TK + a] = __float_as_int(ex / sum);
+        if (hist) atomicAdd(hist + (a / chunk) * E + isel, 1);
     }
 }
 
 cudaError_t launch_topk(const float* part, int S, const float* bias, float* logits_out, int T, int E, int k,
-                        int32_t* blob, uint32_t* err, cudaStream_t stream) {
+                        int32_t* blob, uint32_t* err, cudaStream_t stream, int32_t* hist, int chunk) {
     const int warps = 8;
     dim3 grid((unsigned)cdiv(T, warps)), block(32 * warps);
     const int J = (int)cdiv(E, 32);
 #define MOE_TOPK(JJ)                                                                                        \
     do {                                                                                                    \
-        if (S == 1) topk_kernel<JJ, 1><<<grid, block, 0, stream>>>(part, S, bias, logits_out, T, E, k, blob, err); \
-        else topk_kernel<JJ, (JJ <= 16 ? 8 : 2)><<<grid, block, 0, stream>>>(part, S, bias, logits_out, T, E, k, \
-                                                                            blob, err);                     \
+        if (S == 1)                                                                                         \
+            topk_kernel<JJ, 1><<<grid, block, 0, stream>>>(part, S, bias, logits_out, T, E, k, blob, hist, chunk, err); \
+        else                                                                                                \
+            topk_kernel<JJ, (JJ <= 16 ? 8 : 2)><<<grid, block, 0, stream>>>(part, S, bias, logits_out, T, E, k, \
+                                                                            blob, hist, chunk, err);        \
     } while (0)
     if (J <= 1) MOE_TOPK(1);
     else if (J <= 2) MOE_TOPK(2);

@@ -589,3 +589,24 @@ def test_null_bf16_w_down_is_refused_where_it_is_read(flags):
         L.moe_forward(layer.plan, cw, inp["x"], shape.T, out, None, None, layer.ws)
     assert ei.value.status == L.MOE_ERR_INVALID_ARG
     assert L.moe_launch_count() == l0
+
+
+# ----------------------------------------------- top-k counts the histograms
+
+@pytest.mark.parametrize("T", [5000, 4097])
+def test_topk_counts_the_permutation_histograms(T):
+    """moe_forward where the permutation works in chunks (T*k > 16384): the
+    top-k kernel's per-chunk histograms give the permutation the oracle
+    defines, and the same layer, bit for bit, as the permutation's own
+    histogram pass (MOE_FLAG_TOPK_HIST_OFF)."""
+    shape = synth.SMALL_BF16.with_tokens(T)
+    inp = _dev_inputs(shape, seed=9)
+    fused, out_f, _ = _layer_parity(shape, inp, rows=sample_rows(T, 40, seed=3))
+    plain = MoELayer.from_shape(shape, inp, flags=L.MOE_FLAG_TOPK_HIST_OFF)
+    out_p = plain.forward(inp["x"])
+    plain.check()
+    torch.cuda.synchronize()
+    vf, vp = fused.views(T), plain.views(T)
+    for n in ("blob", "counts", "offsets", "tiles", "inv", "src_tok"):
+        assert torch.equal(vf[n], vp[n]), n
+    assert torch.equal(out_f, out_p)
