@@ -131,6 +131,17 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2 } moe_
  * Remaining Roadmap": fusing the top-k selection).  Results are identical
  * either way; this flag turns the fusion off. */
 #define MOE_FLAG_TOPK_HIST_OFF 0x100u
+/* Fused unpermutation (English page, "Pallas Kernels, SparseCore Co-Design,
+ * and the Roofline": token unpermutation plus the local reduction folded
+ * into the expert path): on the tensor-core paths (bf16 without
+ * MOE_FLAG_DOWN_HILO, and FP8) moe_forward runs the shared expert's down
+ * GEMM last and its epilogue writes out[t] = y_s[t] + sum_j w[t,j] *
+ * y[inv[t*k+j]] directly -- the same order and rounding as the unpermute
+ * kernel, so the output is bit-identical -- instead of storing y_s and
+ * launching the unpermutation.  Off by default: the GEMM epilogue's few
+ * warps keep far fewer loads in flight than the unpermute kernel, so the
+ * gather is slower than the y_s round trip it saves. */
+#define MOE_FLAG_FUSED_COMBINE 0x200u
 
 typedef struct moe_config {
     int32_t T_max;           /* largest token count a call may pass */

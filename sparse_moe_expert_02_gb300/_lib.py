@@ -33,6 +33,7 @@ MOE_FLAG_MCAST_OFF = 0x20
 MOE_FLAG_NARROW_TAILS_ON = 0x40
 MOE_FLAG_NARROW_TAILS_OFF = 0x80
 MOE_FLAG_TOPK_HIST_OFF = 0x100
+MOE_FLAG_FUSED_COMBINE = 0x200
 
 DTYPE_CODE = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8": MOE_FP8_E4M3_B128}
 

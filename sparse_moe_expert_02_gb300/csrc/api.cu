@@ -555,6 +555,7 @@ moe::GroupedGemm down_gemm(const moe_plan* p, const moe_weights* w, int32_t T, W
     g.prefer_pairs = prefer_pairs(p, T);
     g.mcast = prefer_mcast(p, T);
     g.narrow = prefer_narrow(p, T, false);
+    g.many_rows = (int64_t)T * c.top_k >= 64 * (int64_t)c.E;
     g.N = c.D;
     g.Kb = c.I;
     g.Ka = hilo(c) ? 2 * c.I : c.I;  // the hi/lo pair walks W_down twice
@@ -654,6 +655,20 @@ moe_status moe_unpermute(const moe_plan* p, int32_t T, void* out, void* ws, size
     return MOE_OK;
 }
 
+namespace {
+// moe_forward's optional copies of the routing blob and the logits.
+moe_status copy_routing_out(const moe_plan* p, Ws& W, int32_t T, int32_t* blob_out, float* logits_out,
+                            cudaStream_t s) {
+    const moe_config& c = p->cfg;
+    if (blob_out)
+        MOE_CUDA(cudaMemcpyAsync(blob_out, W.at<int32_t>(W.L.blob), (size_t)2 * T * c.top_k * 4,
+                                 cudaMemcpyDeviceToDevice, s));
+    if (logits_out)
+        MOE_CUDA(cudaMemcpyAsync(logits_out, W.at<float>(W.L.logits), (size_t)T * c.E * 4, cudaMemcpyDeviceToDevice, s));
+    return MOE_OK;
+}
+}  // namespace
+
 moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, void* out,
                        int32_t* blob_out, float* logits_out, void* ws, size_t ws_bytes, void* stream) {
     if (p && T == 0) return MOE_OK;  // an empty batch: nothing to read, write or launch
@@ -684,12 +699,27 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
                 moe::gemm_fp8_supported(sdn))
              : (cf.dtype == MOE_BF16 && moe::gemm_tc_supported(gu) && moe::gemm_tc_supported(dn) &&
                 moe::gemm_tc_supported(sgu) && moe::gemm_tc_supported(sdn)));
+    // Fused unpermutation (MOE_FLAG_FUSED_COMBINE, fp16 / bf16 y): the
+    // shared expert's down GEMM runs last, on this stream, and its epilogue
+    // writes out; the unpermute kernel is not launched.
+    const bool fused_comb = overlap && (cf.flags & MOE_FLAG_FUSED_COMBINE) && (fp8 || f16_down(cf));
+    if (fused_comb) {
+        sdn.cmb_out = out;
+        sdn.cmb_out_f32 = cf.out_dtype == MOE_F32;
+        sdn.cmb_blob = W.at<int32_t>(W.L.blob);
+        sdn.cmb_inv = W.at<int32_t>(W.L.inv);
+        sdn.cmb_y = W.at<void>(W.L.y);
+        sdn.cmb_k = cf.top_k;
+        const bool ok = fp8 ? moe::gemm_fp8_supported(sdn) : moe::gemm_tc_supported(sdn);
+        if (!ok) return arg_fail(MOE_ERR_UNSUPPORTED, "fused unpermutation: shape without a kernel");
+    }
     if (overlap) {
         gu.g_end = dn.g_end = cf.E;
         // The FP8 kernel's CTA holds all of an SM's registers, so nothing
         // else runs beside it: the shared GEMMs then take half of the SMs
         // and leave the rest to the top-k and permutation kernels.
         if (fp8) sgu.max_ctas = sdn.max_ctas = std::max(1, p->num_sms / 2);
+        if (fused_comb) sdn.max_ctas = 0;  // it runs alone at the end
         sgu.sched = W.sched(kSchedSharedGateup);
         sdn.sched = W.sched(kSchedSharedDown);
         if (fp8)
@@ -701,7 +731,7 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
         st = route_impl(p, w, x, T, W, stream, fh);
         MOE_CUDA(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
         moe_status side_st = run_gemm(p, sgu, p->side, "shared gate/up GEMM");
-        if (side_st == MOE_OK) side_st = run_gemm(p, sdn, p->side, "shared down GEMM");
+        if (side_st == MOE_OK && !fused_comb) side_st = run_gemm(p, sdn, p->side, "shared down GEMM");
         MOE_CUDA(cudaEventRecord(p->ev_join, p->side));
         if (st == MOE_OK) st = permute_impl(p, x, T, W, s, !fp8, fh);
         if (st == MOE_OK) st = run_gemm(p, gu, s, "gate/up GEMM");
@@ -709,6 +739,10 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
         MOE_CUDA(cudaStreamWaitEvent(s, p->ev_join, 0));  // joined even after an error (stream capture)
         if (side_st != MOE_OK) return side_st;
         if (st != MOE_OK) return st;
+        if (fused_comb) {
+            if ((st = run_gemm(p, sdn, s, "shared down GEMM with the unpermutation")) != MOE_OK) return st;
+            return copy_routing_out(p, W, T, blob_out, logits_out, s);
+        }
     } else {
         if ((st = route_impl(p, w, x, T, W, stream, fh)) != MOE_OK) return st;
         if ((st = permute_impl(p, x, T, W, s, true, fh)) != MOE_OK) return st;
@@ -716,13 +750,7 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
         if ((st = run_gemm(p, dn, s, "down GEMM")) != MOE_OK) return st;
     }
     if ((st = moe_unpermute(p, T, out, ws, ws_bytes, stream)) != MOE_OK) return st;
-    const moe_config& c = cf;
-    if (blob_out)
-        MOE_CUDA(cudaMemcpyAsync(blob_out, W.at<int32_t>(W.L.blob), (size_t)2 * T * c.top_k * 4,
-                                 cudaMemcpyDeviceToDevice, s));
-    if (logits_out)
-        MOE_CUDA(cudaMemcpyAsync(logits_out, W.at<float>(W.L.logits), (size_t)T * c.E * 4, cudaMemcpyDeviceToDevice, s));
-    return MOE_OK;
+    return copy_routing_out(p, W, T, blob_out, logits_out, s);
 }
 
 moe_status moe_pointer_kind(const void* ptr, int32_t* kind) {

@@ -68,6 +68,48 @@ __device__ __forceinline__ float swiglu(float a, float u) { return __fdividef(a 
 
 __host__ __device__ constexpr int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Unpermutation of one 32-column chunk of token t inside a GEMM epilogue:
+// a[i] holds the shared expert's output for columns n0.. (already rounded to
+// y's 16-bit type); it takes w[t,j] * y[inv[t*k+j]] for j = 0..k-1 in order,
+// in fp32 -- the unpermute kernel's order and rounding.  y is [TK, ldy];
+// blob plane 1 (at TK) holds the fp32 weights.  Two slots' loads are in
+// flight at a time.  A dropped pair (row out of range) records
+// MOE_ERR_BOUNDS and contributes nothing.
+template <typename TY>
+__device__ __forceinline__ void combine_chunk32(const TY* __restrict__ y, int64_t ldy, const int32_t* __restrict__ inv,
+                                                const int32_t* __restrict__ blob, int k, int64_t t, int64_t TK, int n0,
+                                                float* a, uint32_t* err) {
+    for (int j0 = 0; j0 < k; j0 += 2) {
+        uint4 q[2][4];
+        float w[2];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            const int j = j0 + s;
+            int r = 0;
+            w[s] = 0.0f;
+            if (j < k) {
+                r = __ldg(inv + t * k + j);
+                w[s] = __int_as_float(__ldg(blob + TK + t * k + j));
+                if ((unsigned)r >= (unsigned)TK) {
+                    record_error(err, MOE_ERR_BOUNDS, (uint32_t)t, (uint32_t)j, 2);
+                    r = 0;
+                    w[s] = 0.0f;
+                }
+            }
+            const uint4* src = (const uint4*)(y + (int64_t)r * ldy + n0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) q[s][v] = j < k ? __ldg(src + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            if (j0 + s >= k) break;
+            const TY* e = (const TY*)q[s];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) a[i] = fmaf(w[s], to_f32(e[i]), a[i]);
+        }
+    }
+}
+
 // Group of a row tile: tiles[g] <= tile < tiles[g+1] (tiles has G+1 entries,
 // nondecreasing).  Binary search, G <= 1025.
 // The same over a copy of the prefix in shared memory.

@@ -44,7 +44,6 @@ namespace f8 {
 
 constexpr int BM = 128;
 constexpr int BKB = 128;                  // K per stage: 128 E4M3 = one 128-byte swizzle row
-constexpr int kStages = 4;
 constexpr int kABytes = BM * BKB;         // 16 KB
 constexpr int kBBytes = 256 * BKB;        // 32 KB
 constexpr int kEpiWarps = 8;
@@ -59,9 +58,25 @@ constexpr uint32_t kBarBytes = 512;  // mbarriers, TMEM address, abort flag, uni
 // Shared copies of the row-tile prefix and the row offsets (G <= 1025
 // groups): the producer finds a unit's group without leaving the SM.
 constexpr int kTabEntries = 1056;
-constexpr uint32_t kSmemBytes = 1024 + kStages * (kABytes + kBBytes) + kBarBytes + 2 * 2 * 128 * 4 + 2 * kTabEntries * 4;
 
 enum Epi : int { EPI_SWIGLU = 0, EPI_PLAIN = 1 };
+
+// Ring depth and shared-memory plan.  The plain (down) epilogue writes
+// 256 B of bf16 y per thread and unit; stored straight from the row-per-lane
+// layout every warp store touches 32 rows, and at prefill sizes those stores
+// throttled the load/store unit (FP8 prefill down 1.20 ms).  With STG the
+// epilogue stages each warp's 32 rows x 64 columns in shared memory and
+// stores 4 rows x 128 B per instruction (1.02 ms); the space comes from a
+// 3-stage ring.  Decode-sized tiles hold a few rows, stream weights from HBM
+// and want the 4-stage ring, so they keep the direct stores.
+constexpr int kStageRow = 144;  // staging row stride in bytes (128 + 16: conflict-free)
+template <int EPI, bool STG> struct Cfg {
+    static constexpr int kStages = (EPI == EPI_PLAIN && STG) ? 3 : 4;
+    static constexpr uint32_t kStagingBytes = (EPI == EPI_PLAIN && STG) ? kEpiWarps * 32 * kStageRow : 0;
+    static constexpr uint32_t kSmemBytes =
+        1024 + kStages * (kABytes + kBBytes) + kBarBytes + 2 * 2 * 128 * 4 + 2 * kTabEntries * 4 + kStagingBytes;
+    static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
+};
 
 struct Params {
     int G, shared_group;
@@ -82,6 +97,13 @@ struct Params {
     float* out_scale;             // SwiGLU: [R, N/128]
     uint32_t* err;
     int64_t spin_ns;
+    // fused unpermutation (plain, single group; see GroupedGemm::cmb_out)
+    void* cmb_out;
+    int cmb_out_f32;
+    const int32_t* cmb_blob;
+    const int32_t* cmb_inv;
+    const void* cmb_y;
+    int cmb_k;
 };
 
 struct Unit {
@@ -107,12 +129,13 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u, const int32_
     return r;
 }
 
-template <int EPI>
+template <int EPI, bool STG>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_fp8_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_a_sh,
                     const __grid_constant__ CUtensorMap tm_b, const __grid_constant__ CUtensorMap tm_b2,
                     const __grid_constant__ CUtensorMap tm_af, const __grid_constant__ CUtensorMap tm_a_shf,
                     const Params p) {
+    constexpr int kStages = Cfg<EPI, STG>::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* sA = smem;
@@ -135,6 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* s_amax = (float*)(smem + kStages * (kABytes + kBBytes) + kBarBytes);  // [2 units][2 halves][128 rows]
     int32_t* s_tiles = (int32_t*)(s_amax + 2 * 2 * 128);
     int32_t* s_off = s_tiles + kTabEntries;
+    uint8_t* s_stage = (uint8_t*)(s_off + kTabEntries);  // plain: [8 warps][32 rows][kStageRow]
     if (p.offsets)
         for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
             s_tiles[i] = __ldg(p.tiles + i);
@@ -448,6 +472,62 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     if (half == 0) p.out_scale[orow * nblocks + un.nb] = sc;
                 }
+            } else if (valid && p.cmb_out) {
+                // fused unpermutation: this row is token orow of the shared group
+                const int64_t TK = (int64_t)p.rows * p.cmb_k;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {  // (unrolled: acc stays in registers)
+                    const int n0 = un.nb * 256 + 128 * half + 32 * cc;
+                    float a[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        a[i] = fmaf(1.0f, __bfloat162float(__float2bfloat16_rn(acc[32 * cc + i])), 0.0f);
+                    combine_chunk32((const bf16*)p.cmb_y, p.N, p.cmb_inv, p.cmb_blob, p.cmb_k, orow, TK, n0, a, p.err);
+                    if (p.cmb_out_f32) {
+                        float* o = (float*)p.cmb_out + orow * p.N + n0;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) *(float4*)(o + i) = make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]);
+                    } else {
+                        bf16* o = (bf16*)p.cmb_out + orow * p.N + n0;
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            uint4 pk;
+                            __nv_bfloat162* h2 = (__nv_bfloat162*)&pk;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) h2[j] = __floats2bfloat162_rn(a[8 * v + 2 * j], a[8 * v + 2 * j + 1]);
+                            *(uint4*)(o + 8 * v) = pk;
+                        }
+                    }
+                }
+            } else if (EPI == EPI_PLAIN && STG) {
+                // y: this warp's 32 rows x 128 columns, in two passes of 64
+                // columns through its shared staging block; on the way out
+                // lane l stores 16 B of row 4i + l/8 (a warp store covers 4
+                // rows x 128 B), only rows of the group.
+                uint8_t* st = s_stage + (size_t)ew * 32 * kStageRow;
+                const int nv = min(32, max(0, un.nrows - (un.m0 + sub * 32)));  // valid rows of the warp
+                const int64_t orow0 = (int64_t)un.row0 + un.m0 + sub * 32;
+#pragma unroll
+                for (int ps = 0; ps < 2; ++ps) {
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        uint4 pk;
+                        __nv_bfloat162* h2 = (__nv_bfloat162*)&pk;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            h2[j] = __floats2bfloat162_rn(acc[64 * ps + 8 * v + 2 * j], acc[64 * ps + 8 * v + 2 * j + 1]);
+                        *(uint4*)(st + lane * kStageRow + 16 * v) = pk;
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = 4 * it + (lane >> 3), ch = lane & 7;
+                        const uint4 pk = *(const uint4*)(st + rr * kStageRow + 16 * ch);
+                        if (rr < nv)
+                            *(uint4*)((bf16*)p.out + (orow0 + rr) * p.ldo + un.nb * 256 + 128 * half + 64 * ps + 8 * ch) = pk;
+                    }
+                    __syncwarp();
+                }
             } else if (valid) {
                 bf16* o = (bf16*)p.out + orow * p.ldo + un.nb * 256 + 128 * half;
 #pragma unroll
@@ -491,25 +571,26 @@ bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, i
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int EPI>
+template <int EPI, bool STG>
 cudaError_t launch_one(int grid, const CUtensorMap& ma, const CUtensorMap& msh, const CUtensorMap& mb,
                        const CUtensorMap& mb2, const CUtensorMap& maf, const CUtensorMap& mshf, const Params& p,
                        cudaStream_t stream) {
     int ready = 0;
-    cudaError_t e = per_device_value((const void*)gemm_fp8_kernel<EPI>, [](int* v) {
+    cudaError_t e = per_device_value((const void*)gemm_fp8_kernel<EPI, STG>, [](int* v) {
         // The warpgroup register split (setmaxnreg) balances only at exactly
         // kRegsLaunch registers per thread; anything else could leave the
         // raising warpgroups waiting for registers that never come free.
         cudaFuncAttributes fa;
-        cudaError_t e2 = cudaFuncGetAttributes(&fa, gemm_fp8_kernel<EPI>);
+        cudaError_t e2 = cudaFuncGetAttributes(&fa, gemm_fp8_kernel<EPI, STG>);
         if (e2 != cudaSuccess) return e2;
         if (fa.numRegs != kRegsLaunch) return cudaErrorInvalidConfiguration;
-        e2 = cudaFuncSetAttribute(gemm_fp8_kernel<EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        e2 = cudaFuncSetAttribute(gemm_fp8_kernel<EPI, STG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  Cfg<EPI, STG>::kSmemBytes);
         if (e2 == cudaSuccess) *v = 1;
         return e2;
     }, &ready);
     if (e != cudaSuccess) return e;
-    gemm_fp8_kernel<EPI><<<grid, kThreads, kSmemBytes, stream>>>(ma, msh, mb, mb2, maf, mshf, p);
+    gemm_fp8_kernel<EPI, STG><<<grid, kThreads, Cfg<EPI, STG>::kSmemBytes, stream>>>(ma, msh, mb, mb2, maf, mshf, p);
     return cudaGetLastError();
 }
 
@@ -521,6 +602,8 @@ bool gemm_fp8_supported(const GroupedGemm& g) {
     if (g.elem != kE4M3 || !tc::encode_fn()) return false;
     if (!g.offsets && (g.rows < 1 || g.a_shared)) return false;  // single group: A only
     if (g.offsets && g.G + 1 > kTabEntries) return false;
+    if (g.cmb_out && (g.offsets || g.b2 || g.cmb_k < 1 || ((uintptr_t)g.cmb_out & 15) || ((uintptr_t)g.cmb_y & 15)))
+        return false;
     if (g.Ka != g.Kb || g.Kb % BKB || g.N % 128) return false;
     if (!g.a_scale || !g.b_scale) return false;
     if (g.b2) {
@@ -556,6 +639,12 @@ cudaError_t launch_gemm_fp8(const GroupedGemm& g, int num_sms, cudaStream_t stre
     p.out_scale = g.out_scale;
     p.err = g.err;
     p.spin_ns = g.spin_ns > 0 ? g.spin_ns : 2000000000LL;
+    p.cmb_out = g.cmb_out;
+    p.cmb_out_f32 = g.cmb_out_f32;
+    p.cmb_blob = g.cmb_blob;
+    p.cmb_inv = g.cmb_inv;
+    p.cmb_y = g.cmb_y;
+    p.cmb_k = g.cmb_k;
     CUtensorMap ma, msh, mb, mb2, maf, mshf;
     if (!make_map_u8(&ma, g.a, g.a_rows, g.Ka, kBoxRowsA)) return cudaErrorInvalidValue;
     if (!make_map_u8(&maf, g.a, g.a_rows, g.Ka, BM)) return cudaErrorInvalidValue;
@@ -575,8 +664,12 @@ cudaError_t launch_gemm_fp8(const GroupedGemm& g, int num_sms, cudaStream_t stre
     const int max_units = g.max_tiles * p.NB;
     if (max_units <= 0) return cudaGetLastError();
     const int grid = std::max(1, std::min(g.max_ctas > 0 ? std::min(num_sms, g.max_ctas) : num_sms, max_units));
-    cudaError_t e = sw ? launch_one<EPI_SWIGLU>(grid, ma, msh, mb, mb2, maf, mshf, p, stream)
-                       : launch_one<EPI_PLAIN>(grid, ma, msh, mb, mb2, maf, mshf, p, stream);
+    // staged y stores where tiles are full (many rows per expert), and in the
+    // fused unpermutation (which writes out itself)
+    const bool stg = !sw && g.many_rows && !g.cmb_out;
+    cudaError_t e = sw ? launch_one<EPI_SWIGLU, false>(grid, ma, msh, mb, mb2, maf, mshf, p, stream)
+                  : stg ? launch_one<EPI_PLAIN, true>(grid, ma, msh, mb, mb2, maf, mshf, p, stream)
+                        : launch_one<EPI_PLAIN, false>(grid, ma, msh, mb, mb2, maf, mshf, p, stream);
     count_launches(1);
     return e;
 }

@@ -73,7 +73,15 @@ constexpr int kBoxRowsA = 16;             // a ragged tile's A rows come in 16-r
 // Shared-memory copy of the group row-tile prefix and row offsets (G <= 1025
 // groups): a unit's group comes from a binary search that never leaves the SM.
 constexpr int kTabEntries = 1056;
-constexpr uint32_t kSmemBytes = 1024 + 196608 + 256 + 2 * kTabEntries * 4;
+// Plain epilogue, 16-bit output: each epilogue warp stages 32 rows x 64
+// columns (128 B per row, rows 144 B apart: conflict-free) in shared memory
+// and stores them 4 rows x 128 B per warp instruction; from the row-per-lane
+// layout every store touched 32 rows, and the down GEMM's 8 KB of y per row
+// (0.74 ms at T=8192, 0.62 ms with the stores left out) waited on them.
+constexpr int kStageRow = 144;
+constexpr uint32_t kStagingBytes = 4 * 32 * kStageRow;
+constexpr uint32_t kSmemBytes = 1024 + 196608 + 256 + 2 * kTabEntries * 4 + kStagingBytes;
+static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
 
 // Stage geometry.  PAIR: A is a bf16 hi/lo pair (hi in columns [0, Kb), lo in
 // [Kb, 2Kb)); a stage holds the hi and lo tiles of one k-block next to one B
@@ -116,6 +124,13 @@ struct Params {
     const float* bias;
     uint32_t* err;
     int64_t spin_ns;
+    // fused unpermutation (see GroupedGemm::cmb_out); cmb_out == nullptr: off
+    void* cmb_out;
+    int cmb_out_f32;
+    const int32_t* cmb_blob;
+    const int32_t* cmb_inv;
+    const void* cmb_y;
+    int cmb_k;
 };
 
 // ------------------------------------------------------------ unit decode
@@ -233,6 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = (uint64_t*)(smem + kRingBytes);
     int32_t* s_tiles = (int32_t*)(smem + kRingBytes + 256);
     int32_t* s_off = s_tiles + kTabEntries;
+    uint8_t* s_stage = (uint8_t*)(s_off + kTabEntries);  // [4 epilogue warps][32 rows][kStageRow]
     if (p.offsets)
         for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
             s_tiles[i] = __ldg(p.tiles + i);
@@ -595,13 +611,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+            } else if (!p.out_f32 && !p.cmb_out && p.BN % 64 == 0) {
+                // 16-bit y through this warp's staging block, 64 columns per pass
+                uint8_t* st = s_stage + (size_t)sub * 32 * kStageRow;
+                const int nv = min(32, max(0, un.nrows - (un.m0 + sub * 32)));  // valid rows of the warp
+                const int64_t orow0 = (int64_t)un.row0 + un.m0 + sub * 32;
+                float mx = 0.f;
+#pragma unroll 1
+                for (int c = 0; c < p.BN; c += 64) {
+                    uint32_t r[64];
+                    tmem_ld32x2(tb + c, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int v = 0; v < 8; ++v) {
+                        uint4 pk;
+                        if (p.out_f16) {
+                            __half2* h2 = (__half2*)&pk;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                const float a = __uint_as_float(r[8 * v + 2 * j]), b = __uint_as_float(r[8 * v + 2 * j + 1]);
+                                mx = fmaxf(mx, fmaxf(fabsf(a), fabsf(b)));
+                                h2[j] = __floats2half2_rn(a, b);
+                            }
+                        } else {
+                            __nv_bfloat162* h2 = (__nv_bfloat162*)&pk;
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                h2[j] = __floats2bfloat162_rn(__uint_as_float(r[8 * v + 2 * j]),
+                                                              __uint_as_float(r[8 * v + 2 * j + 1]));
+                        }
+                        *(uint4*)(st + lane * kStageRow + 16 * v) = pk;
+                    }
+                    __syncwarp();
+                    const int n0 = un.nb * p.BN + c;
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int rr = 4 * it + (lane >> 3), ch = lane & 7;
+                        const uint4 pk = *(const uint4*)(st + rr * kStageRow + 16 * ch);
+                        if (rr < nv) *(uint4*)((uint16_t*)p.out + (orow0 + rr) * p.ldo + n0 + 8 * ch) = pk;
+                    }
+                    __syncwarp();
+                }
+                // (rows past the group hold whatever the stage held: they are
+                // neither stored nor range-checked)
+                if (p.out_f16 && valid && !(mx <= 65504.f)) record_error(p.err, MOE_ERR_NONFINITE, 6, blockIdx.x, 0);
             } else {
 #pragma unroll 1
                 for (int c = 0; c < p.BN; c += 32) {
                     uint32_t r[32];
                     tmem_ld32(tb + c, r);
                     tmem_wait_ld();
-                    if (valid) {
+                    if (valid && p.cmb_out) {
+                        // fused unpermutation: this row is token orow of the shared group
+                        const int n0 = un.nb * p.BN + c;
+                        const int64_t TK = (int64_t)p.rows * p.cmb_k;
+                        float a[32];
+                        float m = 0.f;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float v = p.out_f16 ? __half2float(__float2half_rn(__uint_as_float(r[i])))
+                                                      : __bfloat162float(__float2bfloat16_rn(__uint_as_float(r[i])));
+                            m = fmaxf(m, fabsf(__uint_as_float(r[i])));
+                            a[i] = fmaf(1.0f, v, 0.0f);
+                        }
+                        if (p.out_f16 && !(m <= 65504.f)) record_error(p.err, MOE_ERR_NONFINITE, 6, blockIdx.x, 0);
+                        if (p.out_f16)
+                            combine_chunk32((const f16*)p.cmb_y, p.N, p.cmb_inv, p.cmb_blob, p.cmb_k, orow, TK, n0, a, p.err);
+                        else
+                            combine_chunk32((const bf16*)p.cmb_y, p.N, p.cmb_inv, p.cmb_blob, p.cmb_k, orow, TK, n0, a,
+                                            p.err);
+                        if (p.cmb_out_f32) {
+                            float* o = (float*)p.cmb_out + orow * p.N + n0;
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) *(float4*)(o + i) = make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]);
+                        } else {
+                            store_bf16x32((bf16*)p.cmb_out + orow * p.N + n0, a);
+                        }
+                    } else if (valid) {
                         const int n0 = un.nb * p.BN + c;
                         if (p.out_f32) {
                             float* o = (float*)p.out + un.ks * p.split_stride + orow * p.ldo + n0;
@@ -767,6 +853,11 @@ cudaError_t launch_one(int grid, const Maps& m, const Params& p, cudaStream_t st
 
 bool gemm_tc_supported(const GroupedGemm& g) {
     using namespace tc;
+    if (g.cmb_out) {  // fused unpermutation: one plain group of 16-bit y, 16-byte row segments
+        if (g.offsets || g.b2 || g.Ka != g.Kb || (g.out_elem != kF16 && g.out_elem != kBF16) || g.N % 256 ||
+            g.cmb_k < 1 || !aligned16(g.cmb_out) || !aligned16(g.cmb_y))
+            return false;
+    }
     if (g.elem != kBF16 && g.elem != kF16) return false;
     if (g.b_elem > 0 && g.b_elem != g.elem) return false;  // the tensor cores take one type for A and B
     if (!encode_fn()) return false;
@@ -831,6 +922,12 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     p.bias = g.bias;
     p.err = g.err;
     p.spin_ns = g.spin_ns > 0 ? g.spin_ns : 2000000000LL;
+    p.cmb_out = g.cmb_out;
+    p.cmb_out_f32 = g.cmb_out_f32;
+    p.cmb_blob = g.cmb_blob;
+    p.cmb_inv = g.cmb_inv;
+    p.cmb_y = g.cmb_y;
+    p.cmb_k = g.cmb_k;
 
     // tile pairs: whole weight blocks in pairs (SwiGLU: 128 gate + 128 up;
     // plain: 256-wide), no K split, one A input; static unit order
@@ -838,7 +935,7 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     if (cl) p.sched = nullptr;
     // narrow tails: expert GEMMs with 16-bit outputs in whole 128-feature regions
     p.narrow = g.narrow && !pair && p.KS == 1 && !g.out_pair && !g.bias && g.out_elem != kF32 &&
-               (sw || p.BN % 128 == 0);
+               (sw || p.BN % 128 == 0) && !g.cmb_out;
 
     Maps m;
     const int G = g.offsets ? g.G : 1;

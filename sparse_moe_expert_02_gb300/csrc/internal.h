@@ -42,6 +42,8 @@ struct GroupedGemm {
                                  // operand tiles by TMA multicast) where the shape allows them
     int narrow;                  // bf16/fp16 tensor-core kernel: 1 = tiles of <= 112 valid rows multiplied
                                  // transposed (weights as M, rows as N rounded up to 16)
+    int many_rows;               // FP8 kernel: groups hold many rows (prefill sizes): stage the down
+                                 // GEMM's y stores through shared memory
     int rows;                    // single-group row count
     int max_tiles;               // host bound on the total number of row tiles
     int N;                       // output columns (features) of one group
@@ -69,6 +71,17 @@ struct GroupedGemm {
     int64_t split_stride;
     uint32_t* err;
     int64_t spin_ns;
+    // Fused unpermutation (tensor-core plain epilogue of the shared expert's
+    // down GEMM, single group, row t = token t): instead of storing y_s the
+    // epilogue writes cmb_out[t] = y_s[t] + sum_j w[t,j] * y[cmb_inv[t*k+j]],
+    // y_s rounded to out_elem first and the sum taken in fp32 in slot order,
+    // exactly as the unpermute kernel does.  cmb_out == nullptr: off.
+    void* cmb_out;               // [rows, N]: fp32 (cmb_out_f32) or bf16
+    int cmb_out_f32;
+    const int32_t* cmb_blob;     // [2, rows, k] routing blob (plane 1: fp32 weight bits)
+    const int32_t* cmb_inv;      // [rows * k] grouped row of each (t, j)
+    const void* cmb_y;           // routed expert outputs [rows * k, N], out_elem (fp16 or bf16)
+    int cmb_k;
 };
 
 // Kernel launch accounting (moe_launch_count): every launcher adds the

@@ -490,6 +490,8 @@ def _full_size_parity(shape, inp, host_weights=None, flags=0, out_dtype="f32"):
     counts = v["counts"].cpu().numpy()
     offsets = v["offsets"].cpu().numpy()
     y_rows, e0 = full_size_rows(counts, offsets, T, k)
+    if flags & L.MOE_FLAG_FUSED_COMBINE:  # the shared expert's y rows are folded into out, never stored
+        y_rows = y_rows[y_rows < T * k]
     wsrc = host_weights if host_weights is not None else inp
     ref = y_reference(y_rows, src, offsets, T, k, x, wsrc, shape.dtype, E)
     y = v["y"][torch.as_tensor(y_rows, device="cuda")].double().cpu().numpy()
@@ -521,10 +523,11 @@ def _full_size_parity(shape, inp, host_weights=None, flags=0, out_dtype="f32"):
                                          (synth.BATCHED_DECODE_BF16, L.MOE_FLAG_MCAST_ON),
                                          (synth.PREFILL_BF16, L.MOE_FLAG_NARROW_TAILS_OFF),
                                          (synth.PREFILL_BF16, L.MOE_FLAG_NARROW_TAILS_OFF | L.MOE_FLAG_MCAST_OFF),
-                                         (synth.DECODE_BF16, L.MOE_FLAG_NARROW_TAILS_ON)],
+                                         (synth.DECODE_BF16, L.MOE_FLAG_NARROW_TAILS_ON),
+                                         (synth.PREFILL_BF16, L.MOE_FLAG_FUSED_COMBINE | L.MOE_FLAG_TOPK_HIST_OFF)],
                          ids=["decode", "batched_decode", "prefill", "prefill_cta_pairs", "prefill_no_tile_pairs",
                               "batched_decode_tile_pairs", "prefill_wide_tails", "prefill_plain",
-                              "decode_narrow_tails"])
+                              "decode_narrow_tails", "prefill_fused_unpermute_unfused_hist"])
 def test_full_size_bf16_workloads(shape, flags, big_bf16_weights):
     w_dev, w_host = big_bf16_weights
     inp = _dev_inputs(shape, seed=0, weights=False)
@@ -609,4 +612,33 @@ def test_topk_counts_the_permutation_histograms(T):
     vf, vp = fused.views(T), plain.views(T)
     for n in ("blob", "counts", "offsets", "tiles", "inv", "src_tok"):
         assert torch.equal(vf[n], vp[n]), n
+    assert torch.equal(out_f, out_p)
+
+
+# ------------------------------------------------- fused unpermutation (F1)
+
+FP8_SMALL = synth.LayerShape("fp8_small_T300_D512_E16_I256_k4", 300, 512, 16, 256, 4, "fp8", 1.2)
+
+
+@pytest.mark.parametrize("shape,flags", [(synth.SMALL_BF16, 0), (synth.SMALL_BF16.with_tokens(2000), L.MOE_FLAG_MCAST_ON),
+                                         (synth.SMALL_BF16.with_tokens(129), L.MOE_FLAG_MCAST_OFF),
+                                         (FP8_SMALL, 0), (FP8_SMALL.with_tokens(1), 0)],
+                         ids=["bf16", "bf16_tile_pairs", "bf16_T129", "fp8", "fp8_T1"])
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_fused_unpermutation_is_bit_identical(shape, flags, out_dtype):
+    """MOE_FLAG_FUSED_COMBINE: the shared expert's down GEMM writes out
+    itself, in the unpermute kernel's order and rounding -- the same output
+    bit for bit, and within tolerance of the oracle."""
+    inp = _dev_inputs(shape, seed=11)
+    plain = MoELayer.from_shape(shape, inp, flags=flags, out_dtype=out_dtype)
+    out_p = plain.forward(inp["x"])
+    plain.check()
+    if out_dtype == "f32":  # (a bf16 output's own rounding is not gated against the oracle)
+        fused, out_f, _ = _layer_parity(shape, inp, rows=sample_rows(shape.T, 24, seed=5),
+                                        flags=flags | L.MOE_FLAG_FUSED_COMBINE, out_dtype=out_dtype, check_y=False)
+    else:
+        fused = MoELayer.from_shape(shape, inp, flags=flags | L.MOE_FLAG_FUSED_COMBINE, out_dtype=out_dtype)
+        out_f = fused.forward(inp["x"])
+        fused.check()
+    torch.cuda.synchronize()
     assert torch.equal(out_f, out_p)
