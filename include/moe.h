@@ -105,7 +105,9 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2 } moe_
 /* moe_config.flags */
 #define MOE_FLAG_FORCE_SIMT 0x1u   /* expert GEMMs on the CUDA-core kernel (cross-check path) */
 #define MOE_FLAG_PAIR_CTA_OFF 0x2u /* bf16 expert GEMMs never on CTA pairs (the default) */
-#define MOE_FLAG_PAIR_CTA_ON 0x4u  /* bf16 expert GEMMs on CTA pairs (cta_group::2, 256-row tiles) */
+#define MOE_FLAG_PAIR_CTA_ON 0x4u  /* bf16 expert GEMMs on CTA pairs (cta_group::2, 256-row tiles; a
+                                      group's ragged last tile runs transposed unless
+                                      MOE_FLAG_NARROW_TAILS_OFF) */
 #define MOE_FLAG_DOWN_HILO 0x8u    /* bf16 layer: h as a bf16 hi/lo pair, bf16 W_down (no w_down_f16) */
 /* Tile pairs: the bf16 layer's tensor-core expert GEMMs run on 2-CTA
  * clusters whose CTAs share one operand tile through TMA multicast (two
@@ -232,8 +234,8 @@ MOE_API moe_status moe_quantize_weights(const moe_plan* plan, const float* w, in
  * batch: MOE_OK at once, no pointer is read and nothing is launched).  blob_out (nullable) receives a copy of
  * the [2, T, top_k] routing blob; logits_out (nullable) a copy of the [T, E]
  * fp32 logits.  Clears the workspace error word first.
- * On the tensor-core paths (bf16 and FP8; not MOE_FLAG_FORCE_SIMT or
- * MOE_FLAG_PAIR_CTA_ON) the shared expert's two GEMMs, which need no
+ * On the tensor-core paths (bf16 and FP8; not MOE_FLAG_FORCE_SIMT) the
+ * shared expert's two GEMMs, which need no
  * routing, run on the plan's own stream, forked from `stream` with an event
  * at the start and joined back before the unpermute, so they overlap the
  * router, top-k and permutation; the call stays asynchronous and can be

@@ -240,6 +240,8 @@ int prefer_narrow(const moe_plan* p, int T, bool gateup) {
     const uint32_t f = p->cfg.flags;
     if (f & MOE_FLAG_NARROW_TAILS_OFF) return 0;
     if (f & MOE_FLAG_NARROW_TAILS_ON) return 1;
+    // the CTA-pair kernel stages its transposed stores: narrow tails in both GEMMs
+    if (prefer_pairs(p, T)) return 1;
     return gateup && prefer_mcast(p, T) ? 1 : 0;
 }
 
@@ -694,7 +696,7 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
     // permutation run here; the routed GEMMs then skip the shared group.
     // (FP8: x is quantised first, here, since the shared GEMM reads xq.)
     const bool overlap =
-        !(cf.flags & MOE_FLAG_FORCE_SIMT) && !gu.prefer_pairs &&
+        !(cf.flags & MOE_FLAG_FORCE_SIMT) &&
         (fp8 ? (moe::gemm_fp8_supported(gu) && moe::gemm_fp8_supported(dn) && moe::gemm_fp8_supported(sgu) &&
                 moe::gemm_fp8_supported(sdn))
              : (cf.dtype == MOE_BF16 && moe::gemm_tc_supported(gu) && moe::gemm_tc_supported(dn) &&

@@ -102,9 +102,11 @@ def test_small_fp32_ragged(T):
 
 @pytest.mark.parametrize("flags", [0, L.MOE_FLAG_FORCE_SIMT, L.MOE_FLAG_PAIR_CTA_ON, L.MOE_FLAG_DOWN_HILO,
                                    L.MOE_FLAG_DOWN_HILO | L.MOE_FLAG_FORCE_SIMT, L.MOE_FLAG_MCAST_ON,
-                                   L.MOE_FLAG_NARROW_TAILS_ON, L.MOE_FLAG_NARROW_TAILS_ON | L.MOE_FLAG_MCAST_ON],
+                                   L.MOE_FLAG_NARROW_TAILS_ON, L.MOE_FLAG_NARROW_TAILS_ON | L.MOE_FLAG_MCAST_ON,
+                                   L.MOE_FLAG_PAIR_CTA_ON | L.MOE_FLAG_NARROW_TAILS_OFF,
+                                   L.MOE_FLAG_PAIR_CTA_ON | L.MOE_FLAG_DOWN_HILO],
                          ids=["default", "simt", "cta_pairs", "hilo", "hilo_simt", "tile_pairs", "narrow_tails",
-                              "narrow_tails_tile_pairs"])
+                              "narrow_tails_tile_pairs", "cta_pairs_wide_tails", "cta_pairs_hilo"])
 @pytest.mark.parametrize("T", [300, 1, 128, 129, 700])
 def test_small_bf16_layer(flags, T):
     shape = synth.SMALL_BF16.with_tokens(T)
@@ -524,10 +526,13 @@ def _full_size_parity(shape, inp, host_weights=None, flags=0, out_dtype="f32"):
                                          (synth.PREFILL_BF16, L.MOE_FLAG_NARROW_TAILS_OFF),
                                          (synth.PREFILL_BF16, L.MOE_FLAG_NARROW_TAILS_OFF | L.MOE_FLAG_MCAST_OFF),
                                          (synth.DECODE_BF16, L.MOE_FLAG_NARROW_TAILS_ON),
-                                         (synth.PREFILL_BF16, L.MOE_FLAG_FUSED_COMBINE | L.MOE_FLAG_TOPK_HIST_OFF)],
+                                         (synth.PREFILL_BF16, L.MOE_FLAG_FUSED_COMBINE | L.MOE_FLAG_TOPK_HIST_OFF),
+                                         (synth.PREFILL_BF16, L.MOE_FLAG_PAIR_CTA_ON | L.MOE_FLAG_NARROW_TAILS_OFF),
+                                         (synth.BATCHED_DECODE_BF16, L.MOE_FLAG_PAIR_CTA_ON)],
                          ids=["decode", "batched_decode", "prefill", "prefill_cta_pairs", "prefill_no_tile_pairs",
                               "batched_decode_tile_pairs", "prefill_wide_tails", "prefill_plain",
-                              "decode_narrow_tails", "prefill_fused_unpermute_unfused_hist"])
+                              "decode_narrow_tails", "prefill_fused_unpermute_unfused_hist", "prefill_cta_pairs_wide_tails",
+                              "batched_decode_cta_pairs"])
 def test_full_size_bf16_workloads(shape, flags, big_bf16_weights):
     w_dev, w_host = big_bf16_weights
     inp = _dev_inputs(shape, seed=0, weights=False)
