@@ -29,6 +29,16 @@ __device__ __forceinline__ void record_error(uint32_t* err, uint32_t code, uint3
     }
 }
 
+// Programmatic dependent launch: a kernel launched as a dependent of the
+// previous kernel on its stream may start while that kernel finishes; it
+// waits here before touching anything the earlier kernels write, then lets
+// its own dependents start their prologue.  Without a programmatic
+// dependency both are no-ops.
+__device__ __forceinline__ void pdl_wait_then_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

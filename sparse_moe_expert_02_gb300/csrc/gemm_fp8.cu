@@ -159,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t* s_tiles = (int32_t*)(s_amax + 2 * 2 * 128);
     int32_t* s_off = s_tiles + kTabEntries;
     uint8_t* s_stage = (uint8_t*)(s_off + kTabEntries);  // plain: [8 warps][32 rows][kStageRow]
+    pdl_wait_then_release();
     if (p.offsets)
         for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
             s_tiles[i] = __ldg(p.tiles + i);
@@ -590,8 +591,9 @@ cudaError_t launch_one(int grid, const CUtensorMap& ma, const CUtensorMap& msh, 
         return e2;
     }, &ready);
     if (e != cudaSuccess) return e;
-    gemm_fp8_kernel<EPI, STG><<<grid, kThreads, Cfg<EPI, STG>::kSmemBytes, stream>>>(ma, msh, mb, mb2, maf, mshf, p);
-    return cudaGetLastError();
+    e = launch_kernel(gemm_fp8_kernel<EPI, STG>, dim3(grid), dim3(kThreads), Cfg<EPI, STG>::kSmemBytes, stream, 1, ma,
+                      msh, mb, mb2, maf, mshf, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace f8

@@ -43,6 +43,7 @@ template <typename T> __device__ __forceinline__ void load4(const T* p, float* v
 
 template <typename TE, typename TB, typename TO, bool SWIGLU>
 __global__ void __launch_bounds__(256) gemm_simt_kernel(GroupedGemm g) {
+    pdl_wait_then_release();
     __shared__ float As[BK][BM + 4];
     __shared__ float Bs[BK][BN + 4];
     __shared__ float Bs2[SWIGLU ? BK : 1][BN + 4];
@@ -148,10 +149,11 @@ cudaError_t launch_gemm_simt(const GroupedGemm& g, cudaStream_t stream) {
     dim3 grid((unsigned)std::min(g.max_tiles, 4096), (unsigned)cdiv(g.N, BN)), block(256);
     const bool sw = g.b2 != nullptr;
     const int be = g.b_elem > 0 ? g.b_elem : g.elem;
-#define MOE_SIMT(TA, TBB, TO)                                                          \
-    do {                                                                              \
-        if (sw) gemm_simt_kernel<TA, TBB, TO, true><<<grid, block, 0, stream>>>(g);   \
-        else gemm_simt_kernel<TA, TBB, TO, false><<<grid, block, 0, stream>>>(g);     \
+    cudaError_t e = cudaSuccess;
+#define MOE_SIMT(TA, TBB, TO)                                                                          \
+    do {                                                                                              \
+        if (sw) e = launch_kernel(gemm_simt_kernel<TA, TBB, TO, true>, grid, block, 0, stream, 1, g);  \
+        else e = launch_kernel(gemm_simt_kernel<TA, TBB, TO, false>, grid, block, 0, stream, 1, g);    \
     } while (0)
     if (g.elem == kF32 && be == kF32 && g.out_elem == kF32) MOE_SIMT(float, float, float);
     else if (g.elem == kBF16 && be == kBF16 && g.out_elem == kF32) MOE_SIMT(bf16, bf16, float);
@@ -164,7 +166,7 @@ cudaError_t launch_gemm_simt(const GroupedGemm& g, cudaStream_t stream) {
     else return cudaErrorInvalidValue;
 #undef MOE_SIMT
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace moe

@@ -249,6 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t* s_tiles = (int32_t*)(smem + kRingBytes + 256);
     int32_t* s_off = s_tiles + kTabEntries;
     uint8_t* s_stage = (uint8_t*)(s_off + kTabEntries);  // [4 epilogue warps][32 rows][kStageRow]
+    pdl_wait_then_release();
     if (p.offsets)
         for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
             s_tiles[i] = __ldg(p.tiles + i);
@@ -830,23 +831,11 @@ cudaError_t launch_one(int grid, const Maps& m, const Params& p, cudaStream_t st
         return cudaSuccess;
     }, &ready);
     if (e0 != cudaSuccess) return e0;
-    if (!CL) {
-        kern<<<grid, kThreads, kSmemBytes, stream>>>(m.a, m.a_sh, m.b, m.b2, m.af, m.a_shf, m.ah, m.a_shh, p);
-        return cudaGetLastError();
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * std::max(1, std::min(ready, grid / 2)));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 2;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, m.a, m.a_sh, m.b, m.b2, m.af, m.a_shf, m.ah, m.a_shh, p);
+    if (!CL)
+        return launch_kernel(kern, dim3(grid), dim3(kThreads), kSmemBytes, stream, 1, m.a, m.a_sh, m.b, m.b2, m.af,
+                             m.a_shf, m.ah, m.a_shh, p);
+    return launch_kernel(kern, dim3(2 * std::max(1, std::min(ready, grid / 2))), dim3(kThreads), kSmemBytes, stream, 2,
+                         m.a, m.a_sh, m.b, m.b2, m.af, m.a_shf, m.ah, m.a_shh, p);
 }
 
 }  // namespace tc

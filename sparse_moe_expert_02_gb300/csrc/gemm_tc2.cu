@@ -3,13 +3,13 @@
 // Same computation and epilogues as gemm_tc.cu, for the prefill regime where
 // groups hold hundreds of rows.  A single CTA's 128 x 256 tile reads its
 // whole 32 KB B tile (and 16 KB of A) from shared memory for every 64-wide
-// k-block while TMA writes the same 48 KB in: about 166 bytes of shared-memory
-// traffic per MMA cycle against ~128 the SM serves, so a cta_group::1 tile
-// stays below ~77 % of the tensor pipe.  Two CTAs of a cluster share one
+// k-block while TMA writes the same 48 KB in.  Two CTAs of a cluster share one
 // 256 x 256 tile instead: each loads its own 128 rows of A and half of the B
 // tile (128 of the 256 weight rows), the pair's leader issues M=256 MMAs that
 // read both CTAs' shared memory, and each CTA's TMEM receives its own 128
-// rows x 256 columns: ~110 bytes per MMA cycle per SM, and a 6-stage ring.
+// rows x 256 columns: each SM moves about two thirds of the operand bytes per
+// MMA cycle, and the ring holds 6 stages.  (Measured at T=8192 this was no
+// faster than the single-CTA kernel, so it runs on request only.)
 //   SwiGLU: CTA 0 holds the 128 gate rows, CTA 1 the 128 up rows of the same
 //     features, so accumulator columns 0..127 are gate and 128..255 up in both.
 //   Plain: CTA r holds weight rows nb*256 + r*128 .. +127.
@@ -212,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int32_t* s_off = s_t2 + kTabEntries;
     uint8_t* s_stage = smem + kStageOff;        // [4 epilogue warps][32 rows][kStRow]
     float* s_xchg = (float*)(smem + kXchgOff);  // [2 warp pairs][32 lanes][kXRow]
+    pdl_wait_then_release();
     for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
         s_t2[i] = __ldg(p.tiles2 + i);
         s_off[i] = __ldg(p.offsets + i);
@@ -576,19 +577,8 @@ cudaError_t launch_one(const CUtensorMap& ma, const CUtensorMap& msh, const CUte
     if (e0 != cudaSuccess) return e0;
     int clusters = std::max(1, std::min(max_clusters, max_units));
     if (max_ctas > 0) clusters = std::max(1, std::min(clusters, max_ctas / 2));
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * clusters);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = 2;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ma, msh, mb, mb2, maf, mshf, mbh, mb2h, p);
+    return launch_kernel(kern, dim3(2 * clusters), dim3(kThreads), kSmemBytes, stream, 2, ma, msh, mb, mb2, maf, mshf,
+                         mbh, mb2h, p);
 }
 
 }  // namespace p2

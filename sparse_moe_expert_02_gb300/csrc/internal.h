@@ -97,6 +97,45 @@ void count_launches(int n);
 //   per_device_value: `init` runs once per (key, device) with the lock held;
 //     later calls on that device return the value it produced.
 cudaError_t ensure_smem_attr(const void* func, int bytes);
+
+// Kernels launched while a PdlScope(true) is alive on this host thread are
+// launched as programmatic dependents of the previous kernel on their stream
+// (moe_forward's main-stream chain): they may start their prologue while that
+// kernel finishes and wait for it in pdl_wait_then_release().
+extern thread_local bool t_pdl;
+struct PdlScope {
+    bool prev;
+    explicit PdlScope(bool on) : prev(t_pdl) { t_pdl = on; }
+    ~PdlScope() { t_pdl = prev; }
+};
+// Launch `kern` with the programmatic-dependency attribute when t_pdl is set
+// (plus a cluster dimension when cluster > 1).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          int cluster, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[2];
+    int n = 0;
+    if (cluster > 1) {
+        at[n].id = cudaLaunchAttributeClusterDimension;
+        at[n].val.clusterDim.x = cluster;
+        at[n].val.clusterDim.y = 1;
+        at[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (t_pdl) {
+        at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = at;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kern, args...);
+}
 cudaError_t per_device_value(const void* key, const std::function<cudaError_t(int*)>& init, int* value);
 
 // Launchers (all asynchronous on `stream`; return cudaGetLastError()).

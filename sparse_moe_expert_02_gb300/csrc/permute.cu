@@ -26,6 +26,7 @@ namespace moe {
 
 __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restrict__ idx, int64_t TK, int E,
                                                         int32_t* __restrict__ hist, uint32_t* err) {
+    pdl_wait_then_release();
     extern __shared__ int32_t sh[];
     const int chunk = perm_chunk(TK);
     for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
@@ -68,6 +69,7 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ h
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ tiles, int32_t* __restrict__ tiles2,
                                                          int32_t* __restrict__ shared_src, int64_t TK) {
+    pdl_wait_then_release();
     __shared__ int32_t cnt[1025 + 1];
     __shared__ int32_t ntile[1025 + 1];
     __shared__ int32_t ntile2[1025 + 1];
@@ -125,6 +127,7 @@ __global__ void __launch_bounds__(32 * kRankWarps) perm_rank_kernel(const int32_
                                                                     const int32_t* __restrict__ offsets,
                                                                     int32_t* __restrict__ inv,
                                                                     int32_t* __restrict__ src_tok) {
+    pdl_wait_then_release();
     extern __shared__ int32_t cur[];  // [kRankWarps][E]: counts, then cursors
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunk = perm_chunk(TK);
@@ -194,6 +197,7 @@ __global__ void __launch_bounds__(1024) perm_index_small_kernel(const int32_t* _
                                                                 int32_t* __restrict__ tiles,
                                                                 int32_t* __restrict__ tiles2, int32_t* __restrict__ inv,
                                                                 int32_t* __restrict__ src_tok, uint32_t* err) {
+    pdl_wait_then_release();
     extern __shared__ int32_t sm[];
     int32_t* hist = sm;                   // [32][E]: per-warp counts, then cursors
     int32_t* cnt = hist + 32 * E;         // [E+1]
@@ -270,22 +274,28 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
         cudaError_t e = ensure_smem_attr((const void*)perm_index_small_kernel, kSmallSmem);
         if (e != cudaSuccess) return e;
         const int smem = (32 * E + 4 * (E + 2)) * 4;
-        perm_index_small_kernel<<<1, 1024, smem, stream>>>(idx, T, E, k, counts, offsets, tiles, tiles2, inv, src_tok,
-                                                           err);
+        e = launch_kernel(perm_index_small_kernel, dim3(1), dim3(1024), smem, stream, 1, idx, T, E, k, counts, offsets,
+                          tiles, tiles2, inv, src_tok, err);
         count_launches(1);
-        return cudaGetLastError();
+        return e != cudaSuccess ? e : cudaGetLastError();
     }
     const int nch = (int)cdiv(TK, perm_chunk(TK));
-    if (!hist_ready) perm_hist_kernel<<<nch, 256, E * sizeof(int32_t), stream>>>(idx, TK, E, hist, err);
-    perm_scan_kernel<<<1, 1024, 0, stream>>>(hist, nch, E, T, counts, offsets, tiles, tiles2, src_tok, TK);
+    cudaError_t e = cudaSuccess;
+    if (!hist_ready)
+        e = launch_kernel(perm_hist_kernel, dim3(nch), dim3(256), E * sizeof(int32_t), stream, 1, idx, TK, E, hist, err);
+    if (e == cudaSuccess)
+        e = launch_kernel(perm_scan_kernel, dim3(1), dim3(1024), 0, stream, 1, hist, nch, E, T, counts, offsets, tiles,
+                          tiles2, src_tok, TK);
+    if (e != cudaSuccess) return e;
     const int rank_smem = kRankWarps * E * (int)sizeof(int32_t);
     if (rank_smem > 48 * 1024) {
-        cudaError_t e = ensure_smem_attr((const void*)perm_rank_kernel, rank_smem);
+        e = ensure_smem_attr((const void*)perm_rank_kernel, rank_smem);
         if (e != cudaSuccess) return e;
     }
-    perm_rank_kernel<<<nch, 32 * kRankWarps, rank_smem, stream>>>(idx, TK, k, E, hist, offsets, inv, src_tok);
+    e = launch_kernel(perm_rank_kernel, dim3(nch), dim3(32 * kRankWarps), rank_smem, stream, 1, idx, TK, k, E,
+                      (const int32_t*)hist, (const int32_t*)offsets, inv, src_tok);
     count_launches(hist_ready ? 2 : 3);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- gather
@@ -298,6 +308,7 @@ template <typename V>
 __global__ void __launch_bounds__(256) gather_rows_kernel(const V* __restrict__ x, int64_t row_vecs,
                                                           const int32_t* __restrict__ src_tok, int rows,
                                                           V* __restrict__ xp) {
+    pdl_wait_then_release();
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     for (int r = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
@@ -325,6 +336,7 @@ template <typename V>
 __global__ void __launch_bounds__(256) scatter_rows_kernel(const V* __restrict__ x, int64_t row_vecs,
                                                            const int32_t* __restrict__ inv, int T, int k,
                                                            int64_t rows_out, V* __restrict__ xp) {
+    pdl_wait_then_release();
     const int lane = threadIdx.x & 31;
     const int warps = (gridDim.x * blockDim.x) >> 5;
     for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T; t += warps) {
@@ -356,14 +368,15 @@ cudaError_t launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t*
     if (T <= 0) return cudaGetLastError();
     const int blocks = (int)std::min<int64_t>(cdiv(T, 8), 148 * 16);
     const int64_t rows_out = (int64_t)T * k;
+    cudaError_t e;
     if (row_bytes % 16 == 0)
-        scatter_rows_kernel<int4><<<blocks, 256, 0, stream>>>((const int4*)x, row_bytes / 16, inv, T, k, rows_out,
-                                                             (int4*)xp);
+        e = launch_kernel(scatter_rows_kernel<int4>, dim3(blocks), dim3(256), 0, stream, 1, (const int4*)x,
+                          row_bytes / 16, inv, T, k, rows_out, (int4*)xp);
     else
-        scatter_rows_kernel<int32_t><<<blocks, 256, 0, stream>>>((const int32_t*)x, row_bytes / 4, inv, T, k,
-                                                                rows_out, (int32_t*)xp);
+        e = launch_kernel(scatter_rows_kernel<int32_t>, dim3(blocks), dim3(256), 0, stream, 1, (const int32_t*)x,
+                          row_bytes / 4, inv, T, k, rows_out, (int32_t*)xp);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_gather_rows(const void* x, int elem_bytes, int64_t row_bytes, const int32_t* src_tok, int rows,
@@ -371,13 +384,15 @@ cudaError_t launch_gather_rows(const void* x, int elem_bytes, int64_t row_bytes,
     (void)elem_bytes;
     if (rows <= 0) return cudaGetLastError();
     int blocks = (int)std::min<int64_t>(cdiv(rows, 8), 148 * 16);
+    cudaError_t e;
     if (row_bytes % 16 == 0)
-        gather_rows_kernel<int4><<<blocks, 256, 0, stream>>>((const int4*)x, row_bytes / 16, src_tok, rows, (int4*)xp);
+        e = launch_kernel(gather_rows_kernel<int4>, dim3(blocks), dim3(256), 0, stream, 1, (const int4*)x,
+                          row_bytes / 16, src_tok, rows, (int4*)xp);
     else
-        gather_rows_kernel<int32_t><<<blocks, 256, 0, stream>>>((const int32_t*)x, row_bytes / 4, src_tok, rows,
-                                                               (int32_t*)xp);
+        e = launch_kernel(gather_rows_kernel<int32_t>, dim3(blocks), dim3(256), 0, stream, 1, (const int32_t*)x,
+                          row_bytes / 4, src_tok, rows, (int32_t*)xp);
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // ------------------------------------------------------------- quantisers
@@ -405,6 +420,7 @@ __device__ __forceinline__ void load8f(const float* p, float* v) {
 template <typename T>
 __global__ void __launch_bounds__(256) quant_rows_kernel(const T* __restrict__ x, int rows, int cols,
                                                          uint8_t* __restrict__ q, float* __restrict__ s) {
+    pdl_wait_then_release();
     const int lane = threadIdx.x & 31, sub = lane & 15;
     const int gpr = cols / 128;
     const int64_t ngroups = (int64_t)rows * gpr;

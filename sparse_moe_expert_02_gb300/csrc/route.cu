@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ par
                                                    const float* __restrict__ bias, float* __restrict__ logits_out,
                                                    int T, int E, int k, int32_t* __restrict__ blob,
                                                    int32_t* __restrict__ hist, int chunk, uint32_t* err) {
+    pdl_wait_then_release();
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;  // whole warps leave together
@@ -173,13 +174,15 @@ cudaError_t launch_topk(const float* part, int S, const float* bias, float* logi
     const int warps = 8;
     dim3 grid((unsigned)cdiv(T, warps)), block(32 * warps);
     const int J = (int)cdiv(E, 32);
-#define MOE_TOPK(JJ)                                                                                        \
-    do {                                                                                                    \
-        if (S == 1)                                                                                         \
-            topk_kernel<JJ, 1><<<grid, block, 0, stream>>>(part, S, bias, logits_out, T, E, k, blob, hist, chunk, err); \
-        else                                                                                                \
-            topk_kernel<JJ, (JJ <= 16 ? 8 : 2)><<<grid, block, 0, stream>>>(part, S, bias, logits_out, T, E, k, \
-                                                                            blob, hist, chunk, err);        \
+    cudaError_t e = cudaSuccess;
+#define MOE_TOPK(JJ)                                                                                          \
+    do {                                                                                                      \
+        if (S == 1)                                                                                           \
+            e = launch_kernel(topk_kernel<JJ, 1>, grid, block, 0, stream, 1, part, S, bias, logits_out, T, E, k, \
+                              blob, hist, chunk, err);                                                        \
+        else                                                                                                  \
+            e = launch_kernel(topk_kernel<JJ, (JJ <= 16 ? 8 : 2)>, grid, block, 0, stream, 1, part, S, bias,  \
+                              logits_out, T, E, k, blob, hist, chunk, err);                                   \
     } while (0)
     if (J <= 1) MOE_TOPK(1);
     else if (J <= 2) MOE_TOPK(2);
@@ -189,7 +192,7 @@ cudaError_t launch_topk(const float* part, int S, const float* bias, float* logi
     else MOE_TOPK(32);
 #undef MOE_TOPK
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Compact routing word: one int32 per (t, j) holding the expert index in the

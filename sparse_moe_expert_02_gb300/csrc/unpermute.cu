@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(256) unpermute_kernel(const TY* __restrict__ y
                                                         const int32_t* __restrict__ inv, int T, int D, int k,
                                                         TO* __restrict__ out, uint32_t* err) {
     constexpr int V = 16 / sizeof(TY);  // elements per 16-byte vector of y
+    pdl_wait_then_release();
     __shared__ int64_t rows[33];
     __shared__ float wts[33];
     const int t = blockIdx.x;
@@ -93,8 +94,10 @@ cudaError_t launch_unpermute(const void* y, int y_elem, const int32_t* blob, con
     const int vecs = D / V;
     const int threads = std::min(256, ((vecs + 31) / 32) * 32);
     dim3 grid((unsigned)T, (unsigned)cdiv(vecs, threads));
-#define MOE_UNPERMUTE(TY, TO) \
-    unpermute_kernel<TY, TO><<<grid, threads, 0, stream>>>((const TY*)y, blob, inv, T, D, k, (TO*)out, err)
+    cudaError_t e = cudaSuccess;
+#define MOE_UNPERMUTE(TY, TO)                                                                                \
+    e = launch_kernel(unpermute_kernel<TY, TO>, grid, dim3(threads), 0, stream, 1, (const TY*)y, blob, inv, T, D, k, \
+                      (TO*)out, err)
     const bool o32 = out_elem == kF32;
     if (y_elem == kF32) {
         if (o32) MOE_UNPERMUTE(float, float); else MOE_UNPERMUTE(float, bf16);
@@ -105,7 +108,7 @@ cudaError_t launch_unpermute(const void* y, int y_elem, const int32_t* blob, con
     }
 #undef MOE_UNPERMUTE
     count_launches(1);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // Bounded-wait self-test: one thread waits on an mbarrier that expects an
