@@ -29,6 +29,31 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking probe of the phase of parity `parity`.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// Bounded wait that polls without suspending (the abort flag and the time
+// limit are checked every 256 polls): for the hand-offs on a kernel's
+// critical path, where try_wait's wake-up shows.
+__device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, int64_t limit_ns, volatile int* abort) {
+    uint64_t t0 = 0;
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_test(bar, parity)) return true;
+        if ((i & 255u) == 0) {
+            if (*abort) return false;
+            const uint64_t t = globaltimer_ns();
+            if (t0 == 0) t0 = t;
+            else if ((int64_t)(t - t0) > limit_ns) return false;
+        }
+    }
+}
 // Bounded wait for the phase of parity `parity`; false on timeout or abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int64_t limit_ns, volatile int* abort) {
     if (mbar_try(bar, parity)) return true;
