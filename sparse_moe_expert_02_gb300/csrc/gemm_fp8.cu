@@ -15,7 +15,8 @@
 // Unit, ordering, ring and error handling follow gemm_tc.cu (128 rows x 256
 // accumulator columns; A in 16-row TMA boxes; 4-stage ring of 16 KB A + 32 KB
 // B; bounded waits).  384 threads in three warpgroups: warp 0 TMA, warp 1
-// TMEM + MMA, warps 2-3 idle; warps 4..11 epilogue (two per TMEM lane
+// TMEM + MMA, warps 2-3 copy staged y out (down GEMM at prefill sizes) or
+// idle; warps 4..11 epilogue (two per TMEM lane
 // quarter, each owning half of the columns).  The block launches at 168
 // registers per thread; warpgroup 0 gives back down to 40 and the two
 // epilogue warpgroups take up to 232 (4*32*128 = 8*32*64 registers, so the
@@ -62,17 +63,22 @@ constexpr int kTabEntries = 1056;
 enum Epi : int { EPI_SWIGLU = 0, EPI_PLAIN = 1 };
 
 // Ring depth and shared-memory plan.  The plain (down) epilogue writes
-// 256 B of bf16 y per thread and unit; stored straight from the row-per-lane
-// layout every warp store touches 32 rows, and at prefill sizes those stores
-// throttled the load/store unit (FP8 prefill down 1.20 ms).  With STG the
-// epilogue stages each warp's 32 rows x 64 columns in shared memory and
-// stores 4 rows x 128 B per instruction (1.02 ms); the space comes from a
-// 3-stage ring.  Decode-sized tiles hold a few rows, stream weights from HBM
-// and want the 4-stage ring, so they keep the direct stores.
-constexpr int kStageRow = 144;  // staging row stride in bytes (128 + 16: conflict-free)
+// 256 B of bf16 y per thread and unit.  Stored straight from the
+// row-per-lane layout every warp store touches 32 rows, and at prefill sizes
+// those stores throttled the load/store unit (FP8 prefill down 1.20 ms).
+// With STG the epilogue instead drops the unit's whole 128 x 256 y tile into
+// shared memory (rows kYRow bytes apart) and goes straight on to the next
+// unit; warps 2 and 3 (idle otherwise) copy the tile out, one 512-byte row
+// per warp instruction, while the next unit's slices run, so the 64 KB per
+// unit leave spread over the unit instead of in a burst that held the MMA
+// (FP8 prefill down 1.02 -> 0.92 ms; the epilogue had spent a fifth of its
+// time in the unit-end stores).  The space comes from a 3-stage ring.
+// Decode-sized tiles hold a few rows, stream weights from HBM and want the
+// 4-stage ring, so they keep the direct stores.
+constexpr int kYRow = 528;  // y staging row stride: 512 B + 16 (conflict-free row-per-lane writes)
 template <int EPI, bool STG> struct Cfg {
     static constexpr int kStages = (EPI == EPI_PLAIN && STG) ? 3 : 4;
-    static constexpr uint32_t kStagingBytes = (EPI == EPI_PLAIN && STG) ? kEpiWarps * 32 * kStageRow : 0;
+    static constexpr uint32_t kStagingBytes = (EPI == EPI_PLAIN && STG) ? BM * kYRow : 0;
     static constexpr uint32_t kSmemBytes =
         1024 + kStages * (kABytes + kBBytes) + kBarBytes + 2 * 2 * 128 * 4 + 2 * kTabEntries * 4 + kStagingBytes;
     static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
@@ -158,16 +164,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t xbar0 = smem_u32(bars + 2 * kStages + 5);
     // unit ring: full/empty [4 each] and 4 slots (see gemm_tc.cu)
     const uint32_t ufull0 = smem_u32(bars + 2 * kStages + 13), uempty0 = smem_u32(bars + 2 * kStages + 17);
-    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kStages + 21);
+    // y staging (plain, STG): tile written by the epilogue / copied out by warps 2-3
+    const uint32_t yfull = smem_u32(bars + 2 * kStages + 21), yempty = smem_u32(bars + 2 * kStages + 22);
+    uint32_t* tmem_slot = (uint32_t*)(bars + 2 * kStages + 23);
     volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
     // unit ring slots: [4][6] = unit number, then its decoded group, m0, row0,
     // nrows, nb (the producer decodes each unit once for every role)
     volatile int* s_units = (volatile int*)(tmem_slot + 2);
-    static_assert((2 * kStages + 21) * 8 + 8 + 4 * 6 * 4 <= kBarBytes, "barrier block overflows");
+    // the staged y tile: first global row, valid rows (-1: no more tiles), first column
+    volatile int* s_yinfo = s_units + 4 * 6;
+    static_assert((2 * kStages + 23) * 8 + 8 + 4 * 6 * 4 + 3 * 4 <= kBarBytes, "barrier block overflows");
     float* s_amax = (float*)(smem + kStages * (kABytes + kBBytes) + kBarBytes);  // [2 units][2 halves][128 rows]
     int32_t* s_tiles = (int32_t*)(s_amax + 2 * 2 * 128);
     int32_t* s_off = s_tiles + kTabEntries;
-    uint8_t* s_stage = (uint8_t*)(s_off + kTabEntries);  // plain: [8 warps][32 rows][kStageRow]
+    uint8_t* s_stage = (uint8_t*)(s_off + kTabEntries);  // plain, STG: [128 rows][kYRow]
     pdl_wait_then_release();
     if (p.offsets)
         for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
@@ -186,6 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(cempty0 + 8 * b, kEpiWarps);
         }
         mbar_init(drain, 1);
+        mbar_init(yfull, kEpiWarps);
+        mbar_init(yempty, 2);  // the two copy warps
         for (int b = 0; b < 8; ++b) mbar_init(xbar0 + 8 * b, 2 * 32);
         for (int i = 0; i < 4; ++i) {
             mbar_init(ufull0 + 8 * i, 1);
@@ -329,6 +341,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             volatile int never = 0;
             mbar_wait(drain, 0, 1000000000LL, &never);
         }
+    } else if (EPI == EPI_PLAIN && STG) {
+        // ------------------------------------- y copy-out (warps 2 and 3)
+        // Each staged tile: rows of the group only, warp 2 the even rows,
+        // warp 3 the odd; lane l moves bytes 16l..16l+15 of the row's 512.
+        const int cw = warp - 2;
+        for (uint32_t n = 0;; ++n) {
+            int w_ok = 1;
+            if (lane == 0) {
+                w_ok = mbar_wait(yfull, n & 1u, lim, abort_flag);
+                if (!w_ok) {
+                    record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 18, blockIdx.x, (int)n);
+                    *abort_flag = 1;
+                }
+            }
+            w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+            if (!w_ok) break;
+            const int64_t grow = (int64_t)s_yinfo[0];
+            const int nv = s_yinfo[1], col0 = s_yinfo[2];
+            if (nv < 0) break;
+            for (int r = cw; r < nv; r += 2) {
+                const uint4 v = *(const uint4*)(s_stage + r * kYRow + 16 * lane);
+                *(uint4*)((bf16*)p.out + (grow + r) * p.ldo + col0 + 8 * lane) = v;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(yempty);
+        }
     }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsHigh));
@@ -338,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = ew >> 2;      // which half of the columns
         const int row = sub * 32 + lane;
         uint32_t chunk = 0;
+        uint32_t ny = 0;  // y tiles staged so far (plain, STG)
         bool ok = true;
         for (int i = 0; ok; ++i) {
             int u = -1;  // -1: no more units (or a wait that ran out)
@@ -510,34 +549,35 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             } else if (EPI == EPI_PLAIN && STG) {
-                // y: this warp's 32 rows x 128 columns, in two passes of 64
-                // columns through its shared staging block; on the way out
-                // lane l stores 16 B of row 4i + l/8 (a warp store covers 4
-                // rows x 128 B), only rows of the group.
-                uint8_t* st = s_stage + (size_t)ew * 32 * kStageRow;
-                const int nv = min(32, max(0, un.nrows - (un.m0 + sub * 32)));  // valid rows of the warp
-                const int64_t orow0 = (int64_t)un.row0 + un.m0 + sub * 32;
-#pragma unroll
-                for (int ps = 0; ps < 2; ++ps) {
-#pragma unroll
-                    for (int v = 0; v < 8; ++v) {
-                        uint4 pk;
-                        __nv_bfloat162* h2 = (__nv_bfloat162*)&pk;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            h2[j] = __floats2bfloat162_rn(acc[64 * ps + 8 * v + 2 * j], acc[64 * ps + 8 * v + 2 * j + 1]);
-                        *(uint4*)(st + lane * kStageRow + 16 * v) = pk;
+                // y: this thread's 128 values into row `row` of the staging
+                // tile, once the copy warps are done with the previous one
+                int w_ok = 1;
+                if (lane == 0) {
+                    w_ok = mbar_wait(yempty, (ny & 1u) ^ 1u, lim, abort_flag);
+                    if (!w_ok) {
+                        record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 19, blockIdx.x, u);
+                        *abort_flag = 1;
                     }
-                    __syncwarp();
-#pragma unroll
-                    for (int it = 0; it < 8; ++it) {
-                        const int rr = 4 * it + (lane >> 3), ch = lane & 7;
-                        const uint4 pk = *(const uint4*)(st + rr * kStageRow + 16 * ch);
-                        if (rr < nv)
-                            *(uint4*)((bf16*)p.out + (orow0 + rr) * p.ldo + un.nb * 256 + 128 * half + 64 * ps + 8 * ch) = pk;
-                    }
-                    __syncwarp();
                 }
+                w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+                if (!w_ok) break;
+                uint8_t* st = s_stage + row * kYRow + 256 * half;
+#pragma unroll
+                for (int v = 0; v < 16; ++v) {
+                    uint4 pk;
+                    __nv_bfloat162* h2 = (__nv_bfloat162*)&pk;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) h2[j] = __floats2bfloat162_rn(acc[8 * v + 2 * j], acc[8 * v + 2 * j + 1]);
+                    *(uint4*)(st + 16 * v) = pk;
+                }
+                if (ew == 0 && lane == 0) {
+                    s_yinfo[0] = un.row0 + un.m0;
+                    s_yinfo[1] = min(BM, un.nrows - un.m0);
+                    s_yinfo[2] = un.nb * 256;
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(yfull);
+                ++ny;
             } else if (valid) {
                 bf16* o = (bf16*)p.out + orow * p.ldo + un.nb * 256 + 128 * half;
 #pragma unroll
@@ -548,6 +588,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 4; ++j) h2[j] = __floats2bfloat162_rn(acc[8 * v + 2 * j], acc[8 * v + 2 * j + 1]);
                     *(uint4*)(o + 8 * v) = pk;
                 }
+            }
+        }
+        if (EPI == EPI_PLAIN && STG && !*abort_flag) {
+            // no more tiles: an empty one ends the copy warps' loop
+            int w_ok = 1;
+            if (lane == 0) {
+                w_ok = mbar_wait(yempty, (ny & 1u) ^ 1u, lim, abort_flag);
+                if (!w_ok) {
+                    record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 19, blockIdx.x, -1);
+                    *abort_flag = 1;
+                }
+            }
+            w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+            if (w_ok) {
+                if (ew == 0 && lane == 0) s_yinfo[1] = -1;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(yfull);
             }
         }
     }
