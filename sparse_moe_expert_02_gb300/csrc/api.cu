@@ -460,6 +460,9 @@ moe_status route_impl(const moe_plan* p, const moe_weights* w, const void* x, in
 // once and writes its top_k copies (x leaves DRAM once); below that there
 // are too few tokens to fill the GPU and one warp per output row gathers.
 bool scatter_by_token(int32_t T) { return T >= 1024; }
+// FP8 layer: quantise x on the way into xp (one kernel) where the scatter
+// runs and a row fits the kernel's shared-memory copy
+bool fused_quant_scatter(const moe_config& c, int32_t T) { return scatter_by_token(T) && c.D <= 4096; }
 
 // quant_x: the FP8 layer quantises x into xq here (false when the caller
 // already did).
@@ -474,16 +477,23 @@ moe_status permute_impl(const moe_plan* p, const void* x, int32_t T, Ws& W, cuda
                                        W.at<int32_t>(W.L.src_tok),
                                        W.at<uint32_t>(W.L.err), s, hist_ready));
     if (c.dtype == MOE_FP8_E4M3_B128) {
+        // xq (x quantised) is the shared expert's A operand; the routed rows
+        // are quantised from x on the way into xp at scatter sizes
         if (quant_x)
             MOE_CUDA(moe::launch_quant_rows(x, moe::kBF16, T, c.D, W.at<uint8_t>(W.L.xq), W.at<float>(W.L.xq_scale), s));
-        if (scatter_by_token(T))
-            MOE_CUDA(moe::launch_scatter_rows(W.at<uint8_t>(W.L.xq), c.D, W.at<int32_t>(W.L.inv), T, c.top_k,
-                                              W.at<uint8_t>(W.L.xp), s));
-        else
-            MOE_CUDA(moe::launch_gather_rows(W.at<uint8_t>(W.L.xq), 1, c.D, W.at<int32_t>(W.L.src_tok), TK,
-                                             W.at<uint8_t>(W.L.xp), s));
-        MOE_CUDA(moe::launch_gather_rows(W.at<float>(W.L.xq_scale), 4, (int64_t)(c.D / 128) * 4,
-                                         W.at<int32_t>(W.L.src_tok), TK, W.at<float>(W.L.xp_scale), s));
+        if (fused_quant_scatter(c, T)) {
+            MOE_CUDA(moe::launch_scatter_quant_rows(x, moe::kBF16, T, c.D, W.at<int32_t>(W.L.inv), c.top_k,
+                                                    W.at<uint8_t>(W.L.xp), W.at<float>(W.L.xp_scale), s));
+        } else {
+            if (scatter_by_token(T))
+                MOE_CUDA(moe::launch_scatter_rows(W.at<uint8_t>(W.L.xq), c.D, W.at<int32_t>(W.L.inv), T, c.top_k,
+                                                  W.at<uint8_t>(W.L.xp), s));
+            else
+                MOE_CUDA(moe::launch_gather_rows(W.at<uint8_t>(W.L.xq), 1, c.D, W.at<int32_t>(W.L.src_tok), TK,
+                                                 W.at<uint8_t>(W.L.xp), s));
+            MOE_CUDA(moe::launch_gather_rows(W.at<float>(W.L.xq_scale), 4, (int64_t)(c.D / 128) * 4,
+                                             W.at<int32_t>(W.L.src_tok), TK, W.at<float>(W.L.xp_scale), s));
+        }
     } else {
         const int eb = act_bytes(c.dtype);
         if (scatter_by_token(T))
@@ -737,7 +747,11 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
         if (fused_comb) sdn.max_ctas = 0;  // it runs alone at the end
         sgu.sched = W.sched(kSchedSharedGateup);
         sdn.sched = W.sched(kSchedSharedDown);
-        if (fp8)
+        // FP8: xq (the shared expert's A) is made on the side stream at
+        // scatter sizes, where the permutation quantises the routed rows
+        // itself; below them the gather reads xq, so it is made here
+        const bool side_quant = fp8 && fused_quant_scatter(cf, T);
+        if (fp8 && !side_quant)
             MOE_CUDA(moe::launch_quant_rows(x, moe::kBF16, T, cf.D, W.at<uint8_t>(W.L.xq), W.at<float>(W.L.xq_scale), s));
         MOE_CUDA(cudaEventRecord(p->ev_fork, s));
         // the router GEMM is enqueued first so that it gets the SMs; the
@@ -745,6 +759,9 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
         // top-k and permutation kernels
         st = route_impl(p, w, x, T, W, stream, fh, pdl);
         MOE_CUDA(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
+        if (side_quant)
+            MOE_CUDA(moe::launch_quant_rows(x, moe::kBF16, T, cf.D, W.at<uint8_t>(W.L.xq), W.at<float>(W.L.xq_scale),
+                                            p->side));
         moe_status side_st = run_gemm(p, sgu, p->side, "shared gate/up GEMM");
         if (side_st == MOE_OK && !fused_comb) side_st = run_gemm(p, sdn, p->side, "shared down GEMM");
         MOE_CUDA(cudaEventRecord(p->ev_join, p->side));

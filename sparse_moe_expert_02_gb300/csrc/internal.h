@@ -171,6 +171,10 @@ cudaError_t launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t*
                                 cudaStream_t stream);
 cudaError_t launch_gather_rows(const void* x, int elem_bytes, int64_t row_bytes, const int32_t* src_tok,
                                int rows, void* xp, cudaStream_t stream);
+// FP8 layer, scatter sizes: quantise x per row and 128 columns (as
+// launch_quant_rows) straight into its k rows of xp / xp_scale (inv[t*k+j]).
+cudaError_t launch_scatter_quant_rows(const void* x, int x_elem, int T, int cols, const int32_t* inv, int k,
+                                      uint8_t* xp, float* xp_scale, cudaStream_t stream);
 cudaError_t launch_quant_rows(const void* x, int x_elem, int rows, int cols, uint8_t* q, float* s,
                               cudaStream_t stream);
 cudaError_t launch_quant_blocks(const float* w, int64_t groups, int rows, int cols, uint8_t* q, float* s,

@@ -65,7 +65,7 @@ __device__ void warp_exclusive_scan(const int32_t* v, int n, int32_t* out) {
     if (lane == 31) out[n] = incl;
 }
 
-__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E, int T,
+__global__ void __launch_bounds__(512) perm_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E, int T,
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ tiles, int32_t* __restrict__ tiles2,
                                                          int32_t* __restrict__ shared_src, int64_t TK) {
@@ -76,25 +76,20 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ h
     // the shared expert's rows: token t at grouped row T*k + t
     for (int t = threadIdx.x; t < T; t += blockDim.x) shared_src[TK + t] = t;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        // 8 independent loads in flight per step of the running sum
-        constexpr int U = 8;
+        // 32 independent loads in flight per step of the running sum (the
+        // last step predicated): 3 round trips to L2 for the 80 chunks of
+        // T*k = 81,920 pairs instead of 10
+        constexpr int U = 32;
         int run = 0;
-        int c = 0;
-        for (; c + U <= nchunks; c += U) {
+        for (int c = 0; c < nchunks; c += U) {
             int v[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) v[u] = hist[(int64_t)(c + u) * E + e];
+            for (int u = 0; u < U; ++u) v[u] = (c + u < nchunks) ? hist[(int64_t)(c + u) * E + e] : 0;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                hist[(int64_t)(c + u) * E + e] = run;
+                if (c + u < nchunks) hist[(int64_t)(c + u) * E + e] = run;
                 run += v[u];
             }
-        }
-        for (; c < nchunks; ++c) {
-            const int64_t i = (int64_t)c * E + e;
-            const int v = hist[i];
-            hist[i] = run;
-            run += v;
         }
         cnt[e] = run;
         ntile[e] = (run + kRowTile - 1) / kRowTile;
@@ -284,7 +279,7 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
     if (!hist_ready)
         e = launch_kernel(perm_hist_kernel, dim3(nch), dim3(256), E * sizeof(int32_t), stream, 1, idx, TK, E, hist, err);
     if (e == cudaSuccess)
-        e = launch_kernel(perm_scan_kernel, dim3(1), dim3(1024), 0, stream, 1, hist, nch, E, T, counts, offsets, tiles,
+        e = launch_kernel(perm_scan_kernel, dim3(1), dim3(512), 0, stream, 1, hist, nch, E, T, counts, offsets, tiles,
                           tiles2, src_tok, TK);
     if (e != cudaSuccess) return e;
     const int rank_smem = kRankWarps * E * (int)sizeof(int32_t);
@@ -469,6 +464,96 @@ cudaError_t launch_quant_rows(const void* x, int x_elem, int rows, int cols, uin
         quant_rows_kernel<float><<<blocks, 256, 0, stream>>>((const float*)x, rows, cols, q, s);
     count_launches(1);
     return cudaGetLastError();
+}
+
+// The FP8 layer's permutation at scatter sizes: x is quantised and
+// scattered in one pass.  One warp per token quantises its row two
+// 128-column groups at a time (a half-warp per group, 8 values per lane,
+// four steps of loads in flight) exactly as quant_rows_kernel does (same
+// values, amax, scale and rounding: the codes and scales are
+// bit-identical), into a per-warp copy of the code row and its scales in
+// shared memory; then it writes that copy to each of the token's k rows of
+// xp / xp_scale in 16-byte vectors.  Against quant_rows + scatter of the
+// codes + gather of the scales this reads x once and skips the xq round
+// trip and two launches.
+constexpr int kSqMaxCols = 4096;  // shared row copy per warp (larger D: not supported here)
+constexpr int kSqWarps = 8;
+__global__ void __launch_bounds__(32 * kSqWarps) scatter_quant_rows_kernel(const bf16* __restrict__ x, int Tn, int cols,
+                                                                           const int32_t* __restrict__ inv, int k,
+                                                                           int64_t rows_out, uint8_t* __restrict__ xp,
+                                                                           float* __restrict__ xp_scale) {
+    pdl_wait_then_release();
+    __shared__ __align__(16) uint8_t s_code[kSqWarps][kSqMaxCols];
+    __shared__ float s_sc[kSqWarps][kSqMaxCols / 128];
+    const int lane = threadIdx.x & 31, sub = lane & 15, hw = lane >> 4, w = threadIdx.x >> 5;
+    const int gpr = cols / 128;
+    const int warps = (gridDim.x * blockDim.x) >> 5;
+    for (int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < Tn; t += warps) {
+        const int my = lane < k ? __ldg(inv + (int64_t)t * k + lane) : -1;
+        const bf16* row = x + (int64_t)t * cols;
+        constexpr int B = 4;  // steps (pairs of groups) whose loads are in flight together
+        for (int g0 = 0; g0 < gpr; g0 += 2 * B) {
+            uint4 raw[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int g = g0 + 2 * b + hw;
+                raw[b] = g < gpr ? __ldg((const uint4*)(row + (int64_t)g * 128 + sub * 8)) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int g = g0 + 2 * b + hw;
+                float v[8];
+                const __nv_bfloat162* h2 = (const __nv_bfloat162*)&raw[b];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __bfloat1622float2(h2[i]);
+                    v[2 * i] = f.x;
+                    v[2 * i + 1] = f.y;
+                }
+                float amax = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+                float sc = __fdiv_rn(amax, 448.0f), iv = __fdiv_rn(448.0f, amax);
+                if (amax == 0.0f) { sc = 1.0f; iv = 1.0f; }
+                if (g < gpr) {
+                    uint2 packed;
+                    packed.x = (uint32_t)f32x2_to_e4m3x2(__fmul_rn(v[0], iv), __fmul_rn(v[1], iv)) |
+                               ((uint32_t)f32x2_to_e4m3x2(__fmul_rn(v[2], iv), __fmul_rn(v[3], iv)) << 16);
+                    packed.y = (uint32_t)f32x2_to_e4m3x2(__fmul_rn(v[4], iv), __fmul_rn(v[5], iv)) |
+                               ((uint32_t)f32x2_to_e4m3x2(__fmul_rn(v[6], iv), __fmul_rn(v[7], iv)) << 16);
+                    *(uint2*)(&s_code[w][g * 128 + sub * 8]) = packed;
+                    if (sub == 0) s_sc[w][g] = sc;
+                }
+            }
+        }
+        __syncwarp();
+        const int nvec = cols / 16;  // 16-byte vectors of the code row
+        for (int j = 0; j < k; ++j) {
+            const int r = __shfl_sync(0xffffffffu, my, j);
+            if (r < 0 || r >= rows_out) continue;
+            uint8_t* dst = xp + (int64_t)r * cols;
+            for (int i = lane; i < nvec; i += 32) __stcs((uint4*)(dst + 16 * i), *(const uint4*)(&s_code[w][16 * i]));
+            for (int g = lane; g < gpr; g += 32) xp_scale[(int64_t)r * gpr + g] = s_sc[w][g];
+        }
+        __syncwarp();
+    }
+}
+
+cudaError_t launch_scatter_quant_rows(const void* x, int x_elem, int T, int cols, const int32_t* inv, int k,
+                                      uint8_t* xp, float* xp_scale, cudaStream_t stream) {
+    if (T <= 0) return cudaGetLastError();
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int blocks = (int)std::min<int64_t>(cdiv(T, 8), (int64_t)std::max(1, sms) * 16);
+    const int64_t rows_out = (int64_t)T * k;
+    if (x_elem != kBF16 || cols > kSqMaxCols || cols % 128) return cudaErrorInvalidValue;  // bf16 x, D <= 4096
+    cudaError_t e = launch_kernel(scatter_quant_rows_kernel, dim3(blocks), dim3(32 * kSqWarps), 0, stream, 1, (const bf16*)x,
+                                  T, cols, inv, k, rows_out, xp, xp_scale);
+    count_launches(1);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // One block per 128x128 weight block of a [groups, rows, cols] fp32 tensor.
