@@ -22,6 +22,19 @@
 
 namespace moe {
 
+// SM count of the current device (looked up once per device): the grid cap
+// of the grid-stride copy kernels below.
+static int current_sms() {
+    static const char key = 0;
+    int v = 0;
+    const cudaError_t e = per_device_value(&key, [](int* out) {
+        int dev = 0;
+        cudaError_t e2 = cudaGetDevice(&dev);
+        return e2 != cudaSuccess ? e2 : cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev);
+    }, &v);
+    return (e == cudaSuccess && v > 0) ? v : 1;
+}
+
 // ------------------------------------------------------------------ hist
 
 __global__ void __launch_bounds__(256) perm_hist_kernel(const int32_t* __restrict__ idx, int64_t TK, int E,
@@ -361,7 +374,7 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const V* __restrict__
 cudaError_t launch_scatter_rows(const void* x, int64_t row_bytes, const int32_t* inv, int T, int k, void* xp,
                                 cudaStream_t stream) {
     if (T <= 0) return cudaGetLastError();
-    const int blocks = (int)std::min<int64_t>(cdiv(T, 8), 148 * 16);
+    const int blocks = (int)std::min<int64_t>(cdiv(T, 8), (int64_t)current_sms() * 16);
     const int64_t rows_out = (int64_t)T * k;
     cudaError_t e;
     if (row_bytes % 16 == 0)
@@ -378,7 +391,7 @@ cudaError_t launch_gather_rows(const void* x, int elem_bytes, int64_t row_bytes,
                                void* xp, cudaStream_t stream) {
     (void)elem_bytes;
     if (rows <= 0) return cudaGetLastError();
-    int blocks = (int)std::min<int64_t>(cdiv(rows, 8), 148 * 16);
+    int blocks = (int)std::min<int64_t>(cdiv(rows, 8), (int64_t)current_sms() * 16);
     cudaError_t e;
     if (row_bytes % 16 == 0)
         e = launch_kernel(gather_rows_kernel<int4>, dim3(blocks), dim3(256), 0, stream, 1, (const int4*)x,
@@ -457,7 +470,7 @@ cudaError_t launch_quant_rows(const void* x, int x_elem, int rows, int cols, uin
                               cudaStream_t stream) {
     if (rows <= 0) return cudaGetLastError();
     int64_t groups = (int64_t)rows * (cols / 128);
-    int blocks = (int)std::min<int64_t>(cdiv(groups, 16), 148 * 32);
+    int blocks = (int)std::min<int64_t>(cdiv(groups, 16), (int64_t)current_sms() * 32);
     if (x_elem == kBF16)
         quant_rows_kernel<bf16><<<blocks, 256, 0, stream>>>((const bf16*)x, rows, cols, q, s);
     else
@@ -544,10 +557,7 @@ __global__ void __launch_bounds__(32 * kSqWarps) scatter_quant_rows_kernel(const
 cudaError_t launch_scatter_quant_rows(const void* x, int x_elem, int T, int cols, const int32_t* inv, int k,
                                       uint8_t* xp, float* xp_scale, cudaStream_t stream) {
     if (T <= 0) return cudaGetLastError();
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int blocks = (int)std::min<int64_t>(cdiv(T, 8), (int64_t)std::max(1, sms) * 16);
+    const int blocks = (int)std::min<int64_t>(cdiv(T, 8), (int64_t)current_sms() * 16);
     const int64_t rows_out = (int64_t)T * k;
     if (x_elem != kBF16 || cols > kSqMaxCols || cols % 128) return cudaErrorInvalidValue;  // bf16 x, D <= 4096
     cudaError_t e = launch_kernel(scatter_quant_rows_kernel, dim3(blocks), dim3(32 * kSqWarps), 0, stream, 1, (const bf16*)x,
