@@ -269,6 +269,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = CL ? (int)cluster_rank() : 0;
+    // a timed-out wait stops this CTA's roles, and under tile pairs the peer's
+    auto abort_cta = [&](volatile int* f) {
+        if (CL) raise_abort_pair(f, (uint32_t)rank);
+        else *f = 1;
+    };
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(full0 + 8 * s, 1);
@@ -324,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (u >= 0) next_u = p.sched ? atomicAdd(p.sched, 1) : ord0 + (i + 1) * ordn;
                 if (!mbar_wait(uempty0 + 8 * (i & 3), ((i >> 2) & 1) ^ 1, lim, abort_flag)) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 5, blockIdx.x, i);
-                    *abort_flag = 1;
+                    abort_cta(abort_flag);
                     ok = false;
                     break;
                 }
@@ -351,7 +356,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = un.ks * kbs; kb < (un.ks + 1) * kbs; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, lim, abort_flag)) {
                         record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 1, blockIdx.x, u);
-                        *abort_flag = 1;
+                        abort_cta(abort_flag);
                         ok = false;
                         break;
                     }
@@ -398,12 +403,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) {  // let every copy this thread started land before the CTA exits
-                for (int s = 0; s < kStages; ++s)
-                    if (armed & (1u << s)) {
-                        volatile int never = 0;
-                        mbar_wait(full0 + 8 * s, (armed_parity >> s) & 1u, 1000000000LL, &never);
-                    }
-                if (CL) sleep_ns(200000);  // and the halves it sent to the peer
+                if (CL) {
+                    // (a tile-pair stage also waits for the peer's half, which an
+                    // aborted peer may never send: give this CTA's own copies,
+                    // here and in the peer, time to land instead)
+                    sleep_ns(200000);
+                } else {
+                    for (int s = 0; s < kStages; ++s)
+                        if (armed & (1u << s)) {
+                            volatile int never = 0;
+                            mbar_wait(full0 + 8 * s, (armed_parity >> s) & 1u, 1000000000LL, &never);
+                        }
+                }
             }
         }
     } else if (warp == 1) {
@@ -416,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; ok; ++i) {
                 if (!mbar_wait(ufull0 + 8 * (i & 3), (i >> 2) & 1, lim, abort_flag)) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 6, blockIdx.x, i);
-                    *abort_flag = 1;
+                    abort_cta(abort_flag);
                     break;
                 }
                 const int u = s_units[i & 3];
@@ -435,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int regions = (EPI == EPI_SWIGLU) ? 2 : p.BN / 128;
                 if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, lim, abort_flag)) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 2, blockIdx.x, u);
-                    *abort_flag = 1;
+                    abort_cta(abort_flag);
                     ok = false;
                     break;
                 }
@@ -444,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < kbs; ++kb) {
                     if (!mbar_wait(full0 + 8 * stage, phase, lim, abort_flag)) {
                         record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 3, blockIdx.x, u);
-                        *abort_flag = 1;
+                        abort_cta(abort_flag);
                         ok = false;
                         break;
                     }
@@ -506,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(uempty0 + 8 * (i & 3));
                 } else {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 7, blockIdx.x, i);
-                    *abort_flag = 1;
+                    abort_cta(abort_flag);
                 }
             }
             got = __shfl_sync(0xffffffffu, got, 0);
@@ -520,7 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(tfull0 + 8 * acc, acc_phase, lim, abort_flag);
                 if (!ok) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 4, blockIdx.x, u);
-                    *abort_flag = 1;
+                    abort_cta(abort_flag);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);

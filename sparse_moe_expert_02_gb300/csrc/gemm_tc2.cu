@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, lim, abort_flag)) {
                         record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 21, blockIdx.x, u);
-                        *abort_flag = 1;
+                        raise_abort_pair(abort_flag, rank);
                         aborted = true;
                         break;
                     }
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t idesc = p.in_f16 ? idesc_f16(2 * BM, n) : idesc_bf16(2 * BM, n);
                 if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, lim, abort_flag)) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 22, blockIdx.x, u);
-                    *abort_flag = 1;
+                    raise_abort_pair(abort_flag, rank);
                     aborted = true;
                     break;
                 }
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(full0 + 8 * stage, phase, lim, abort_flag)) {
                         record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 23, blockIdx.x, u);
-                        *abort_flag = 1;
+                        raise_abort_pair(abort_flag, rank);
                         aborted = true;
                         break;
                     }
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = mbar_wait(tfull0 + 8 * acc, acc_phase, lim, abort_flag);
                 if (!ok) {
                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 24, blockIdx.x, u);
-                    *abort_flag = 1;
+                    raise_abort_pair(abort_flag, rank);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!w_ok) {
                                 if (lane == 0) {
                                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 25, blockIdx.x, u);
-                                    *abort_flag = 1;
+                                    raise_abort_pair(abort_flag, rank);
                                 }
                                 aborted = true;
                                 break;
@@ -438,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (!w_ok) {
                                 if (lane == 0) {
                                     record_error(p.err, MOE_ERR_DEVICE_TIMEOUT, 26, blockIdx.x, u);
-                                    *abort_flag = 1;
+                                    raise_abort_pair(abort_flag, rank);
                                 }
                                 aborted = true;
                                 break;

@@ -54,6 +54,18 @@ __device__ __forceinline__ bool mbar_spin(uint32_t bar, uint32_t parity, int64_t
         }
     }
 }
+// Abort flag of a CTA in a 2-CTA cluster: set it here and in the peer CTA
+// (same shared-memory offset), so that the peer's waits end on the flag
+// rather than each running out its own limit.  The peer is still resident:
+// both CTAs meet at a cluster barrier before either exits.
+__device__ __forceinline__ void raise_abort_pair(volatile int* flag, uint32_t rank) {
+    *flag = 1;
+    uint32_t peer;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                 : "=r"(peer)
+                 : "r"((uint32_t)__cvta_generic_to_shared((const void*)flag)), "r"(rank ^ 1u));
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(peer), "r"(1) : "memory");
+}
 // Bounded wait for the phase of parity `parity`; false on timeout or abort.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int64_t limit_ns, volatile int* abort) {
     if (mbar_try(bar, parity)) return true;

@@ -355,6 +355,33 @@ def test_bounded_wait_times_out_and_reports():
     assert float(torch.ones(4, device="cuda").sum()) == 4.0
 
 
+@pytest.mark.parametrize("shape,flags", [(synth.SMALL_BF16.with_tokens(2000), L.MOE_FLAG_MCAST_ON),
+                                         (synth.SMALL_BF16.with_tokens(700), L.MOE_FLAG_PAIR_CTA_ON),
+                                         (synth.SMALL_BF16.with_tokens(300), 0),
+                                         (synth.SMALL_FP8.with_tokens(1500), 0)],
+                         ids=["bf16_tile_pairs", "bf16_cta_pairs", "bf16_one_cta", "fp8"])
+def test_gemm_waits_that_run_out_end_the_kernels_cleanly(shape, flags):
+    """A 1 ns wait limit makes every GEMM hand-off that is not ready at once
+    run out: the kernels record MOE_ERR_DEVICE_TIMEOUT, stop their roles (in
+    2-CTA clusters the peer too), let their copies land, free TMEM and
+    return; the status reaches the host and the context still runs a correct
+    forward."""
+    inp = _dev_inputs(shape, seed=14)
+    hurried = MoELayer.from_shape(shape, inp, flags=flags, out_dtype="bf16", spin_limit_ns=1)
+    hurried.forward(inp["x"])
+    torch.cuda.synchronize()
+    assert L.moe_check_status(hurried.plan, hurried.ws) == L.MOE_ERR_DEVICE_TIMEOUT
+    normal = MoELayer.from_shape(shape, inp, flags=flags, out_dtype="bf16")
+    out = normal.forward(inp["x"])
+    normal.check()
+    again = MoELayer.from_shape(shape, inp, flags=flags, out_dtype="bf16")
+    out2 = again.forward(inp["x"])
+    again.check()
+    torch.cuda.synchronize()
+    assert torch.equal(out, out2)
+    assert torch.isfinite(out).all()
+
+
 def test_nonfinite_logit_is_reported():
     shape = synth.SMALL_BF16.with_tokens(40)
     inp = _dev_inputs(shape, seed=7)
