@@ -706,7 +706,7 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
     // The shared expert needs no routing: on the tensor-core path its two
     // GEMMs run on the plan's second stream while the router, top-k and
     // permutation run here; the routed GEMMs then skip the shared group.
-    // (FP8: x is quantised first, here, since the shared GEMM reads xq.)
+    // (FP8: the shared GEMM reads xq, x quantised per row; see below.)
     const bool overlap =
         !(cf.flags & MOE_FLAG_FORCE_SIMT) &&
         (fp8 ? (moe::gemm_fp8_supported(gu) && moe::gemm_fp8_supported(dn) && moe::gemm_fp8_supported(sgu) &&
