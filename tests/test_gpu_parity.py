@@ -455,10 +455,18 @@ def test_empty_batch_is_a_no_op():
 
 # ------------------------------------------------------------- FP8 layer
 
-@pytest.mark.parametrize("T", [300, 1, 129, 1500, 5000])
+@pytest.mark.parametrize("T", [300, 1, 129, 1023, 1024, 1500, 5000])
 def test_small_fp8_layer(T):
+    # (from 1024 tokens the permutation quantises x on the way into xp)
     shape = synth.SMALL_FP8.with_tokens(T)
     _layer_parity(shape, _dev_inputs(shape, seed=9), out_dtype="bf16")
+
+
+def test_fp8_layer_wider_than_the_fused_permutation():
+    """D = 4352 (> 4096) at scatter sizes: the permutation falls back to
+    quantising x into xq and scattering codes and scales separately."""
+    shape = synth.LayerShape("fp8_T1024_D4352_E8_I128_k2", 1024, 4352, 8, 128, 2, "fp8", 1.2)
+    _layer_parity(shape, _dev_inputs(shape, seed=16), rows=sample_rows(shape.T, 48, seed=2), out_dtype="bf16")
 
 
 def test_fp8_h_codes_mostly_match_oracle():
