@@ -144,6 +144,16 @@ typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3_B128 = 2 } moe_
  * warps keep far fewer loads in flight than the unpermute kernel, so the
  * gather is slower than the y_s round trip it saves. */
 #define MOE_FLAG_FUSED_COMBINE 0x200u
+/* Split expert GEMMs (bf16 layer, prefill sizes: T*top_k >= 64*E, on the
+ * tensor-core path with the shared expert on the second stream): each routed
+ * expert GEMM runs as two concurrent launches -- the whole 256-row pairs of
+ * every group on CTA pairs (M=256 MMAs, which spend less time per k-block
+ * waiting for operands than single CTAs), and the remaining rows of each
+ * group as 128-row tiles on single CTAs on the second stream.  How many CTA
+ * pairs take part is computed on the device from the group sizes (the rest
+ * exit at once and leave their SMs to the single-CTA launch).  Results are
+ * bit-identical either way; this flag turns the split off. */
+#define MOE_FLAG_SPLIT_GEMM_OFF 0x400u
 
 typedef struct moe_config {
     int32_t T_max;           /* largest token count a call may pass */
@@ -200,6 +210,10 @@ typedef struct moe_ws_layout {
                           fp16 (MOE_BF16) or bf16 (FP8 layer) */
     size_t logits_part;/* f32 [S, T, E] router K-slice partials when T is small (S > 1), else 0 */
     size_t tiles2;     /* int32 [E+2]: exclusive prefix of ceil(counts/256) (row-tile pairs) */
+    size_t pairs;      /* int32 [2, E+2] then [2]: exclusive prefixes of floor(counts/256) (whole
+                          256-row pairs) and of the 128-row tiles of what remains of each group,
+                          then the CTA-pair clusters the split expert GEMMs run with (gate/up,
+                          down); written by the permutation (see MOE_FLAG_SPLIT_GEMM_OFF) */
 } moe_ws_layout;
 
 /* Validate a configuration and build a host-side plan for `device`.

@@ -34,6 +34,7 @@ MOE_FLAG_NARROW_TAILS_ON = 0x40
 MOE_FLAG_NARROW_TAILS_OFF = 0x80
 MOE_FLAG_TOPK_HIST_OFF = 0x100
 MOE_FLAG_FUSED_COMBINE = 0x200
+MOE_FLAG_SPLIT_GEMM_OFF = 0x400
 
 DTYPE_CODE = {"f32": MOE_F32, "bf16": MOE_BF16, "fp8": MOE_FP8_E4M3_B128}
 
@@ -61,7 +62,7 @@ class moe_weights(ctypes.Structure):
 class moe_ws_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("total", "err", "logits", "blob", "counts", "offsets", "tiles", "inv", "src_tok", "hist", "xq",
-                 "xq_scale", "xp", "xp_scale", "h", "h_scale", "y", "logits_part", "tiles2")]
+                 "xq_scale", "xp", "xp_scale", "h", "h_scale", "y", "logits_part", "tiles2", "pairs")]
 
 
 class MoEError(RuntimeError):

@@ -64,6 +64,9 @@ struct moe_plan {
     // joined back into the caller's stream with these events
     cudaStream_t side = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+    // split expert GEMMs: the permutation is done (the second stream starts
+    // the single-CTA halves)
+    cudaEvent_t ev_perm = nullptr;
 };
 
 namespace {
@@ -142,6 +145,7 @@ void layout(const moe_config& c, int num_sms, int T, moe_ws_layout* L) {
     const int S = route_splits(c, T, num_sms);
     L->logits_part = S > 1 ? take((size_t)S * T * c.E * 4) : 0;
     L->tiles2 = take((size_t)(c.E + 2) * 4);
+    L->pairs = take((size_t)(2 * (c.E + 2) + 2) * 4);
     L->total = o;
 }
 
@@ -313,7 +317,8 @@ moe_status moe_plan_create(const moe_config* cfg, int device, moe_plan** out) {
     if (cudaSetDevice(device) != cudaSuccess ||
         cudaStreamCreateWithFlags(&p->side, cudaStreamNonBlocking) != cudaSuccess ||
         cudaEventCreateWithFlags(&p->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaEventCreateWithFlags(&p->ev_join, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&p->ev_perm, cudaEventDisableTiming) != cudaSuccess) {
         moe_plan_destroy(p);
         cudaSetDevice(prev);
         return arg_fail(MOE_ERR_CUDA, "stream or event creation failed");
@@ -327,6 +332,7 @@ void moe_plan_destroy(moe_plan* p) {
     if (!p) return;
     if (p->ev_fork) cudaEventDestroy(p->ev_fork);
     if (p->ev_join) cudaEventDestroy(p->ev_join);
+    if (p->ev_perm) cudaEventDestroy(p->ev_perm);
     if (p->side) cudaStreamDestroy(p->side);
     delete p;
 }
@@ -475,7 +481,8 @@ moe_status permute_impl(const moe_plan* p, const void* x, int32_t T, Ws& W, cuda
                                        W.at<int32_t>(W.L.counts), W.at<int32_t>(W.L.offsets),
                                        W.at<int32_t>(W.L.tiles), W.at<int32_t>(W.L.tiles2), W.at<int32_t>(W.L.inv),
                                        W.at<int32_t>(W.L.src_tok),
-                                       W.at<uint32_t>(W.L.err), s, hist_ready));
+                                       W.at<uint32_t>(W.L.err), s, hist_ready, W.at<int32_t>(W.L.pairs),
+                                       std::max(1, p->num_sms / 2), prefer_narrow(p, T, true)));
     if (c.dtype == MOE_FP8_E4M3_B128) {
         // xq (x quantised) is the shared expert's A operand; the routed rows
         // are quantised from x on the way into xp at scatter sizes
@@ -635,6 +642,37 @@ moe::GroupedGemm shared_only(const moe::GroupedGemm& full, const moe_config& c, 
     return g;
 }
 
+// Split expert GEMMs (see moe_forward): the bf16 layer at prefill sizes,
+// unless the caller asked for the plain CTA-pair kernel or turned the split
+// off.  Fills the two launches of each GEMM: gp on CTA pairs over the whole
+// 256-row pairs (pairs[0..E+1]), as many pairs as the permutation counted
+// (pairs[2(E+2) + i]); gr on single CTAs over the rest of each group
+// (pairs[E+2..]), drawing units from the shared expert's counters (its GEMMs
+// are done by then on the same stream).
+bool split_wanted(const moe_plan* p, int T, Ws& W, const moe::GroupedGemm& gu, const moe::GroupedGemm& dn,
+                  moe::GroupedGemm* gp, moe::GroupedGemm* gr) {
+    const moe_config& c = p->cfg;
+    if (c.flags & (MOE_FLAG_SPLIT_GEMM_OFF | MOE_FLAG_PAIR_CTA_ON | MOE_FLAG_FORCE_SIMT)) return false;
+    if (!f16_down(c) || (int64_t)T * c.top_k < 64LL * c.E) return false;
+    int32_t* pairs = W.at<int32_t>(W.L.pairs);
+    for (int i = 0; i < 2; ++i) {
+        const moe::GroupedGemm& base = i == 0 ? gu : dn;
+        gp[i] = base;
+        gp[i].prefer_pairs = 1;
+        gp[i].tiles2 = pairs;
+        gp[i].narrow = 0;
+        gp[i].pair_active = pairs + 2 * (c.E + 2) + i;
+        gr[i] = base;
+        gr[i].tiles = pairs + (c.E + 2);
+        gr[i].rem_only = 1;
+        gr[i].mcast = 0;
+        gr[i].prefer_pairs = 0;
+        gr[i].sched = W.sched(i == 0 ? kSchedSharedGateup : kSchedSharedDown);
+        if (!moe::gemm_tc2_supported(gp[i]) || !moe::gemm_tc_supported(gr[i])) return false;
+    }
+    return true;
+}
+
 }  // namespace
 
 moe_status moe_gemm_gateup(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, void* ws,
@@ -766,14 +804,32 @@ moe_status moe_forward(const moe_plan* p, const moe_weights* w, const void* x, i
                                             p->side));
         moe_status side_st = run_gemm(p, sgu, p->side, "shared gate/up GEMM");
         if (side_st == MOE_OK && !fused_comb) side_st = run_gemm(p, sdn, p->side, "shared down GEMM");
-        MOE_CUDA(cudaEventRecord(p->ev_join, p->side));
+        // Split expert GEMMs (MOE_FLAG_SPLIT_GEMM_OFF): each routed GEMM as the
+        // whole 256-row pairs on CTA pairs here and the rest of every group on
+        // single CTAs on the second stream, at the same time.  The two halves
+        // write disjoint rows, and each down half reads only the h rows its
+        // own gate/up half wrote.  Prefill bf16, T=8192: see the design notes.
+        moe::GroupedGemm gp[2], gr[2];
+        const bool split = !fp8 && !fused_comb && split_wanted(p, T, W, gu, dn, gp, gr);
+        if (!split) MOE_CUDA(cudaEventRecord(p->ev_join, p->side));
         {
             // the main-stream chain after the top-k: each kernel a programmatic
             // dependent of the one before it
             moe::PdlScope scope(pdl);
             if (st == MOE_OK) st = permute_impl(p, x, T, W, s, !fp8, fh);
-            if (st == MOE_OK) st = run_gemm(p, gu, s, "gate/up GEMM");
-            if (st == MOE_OK) st = run_gemm(p, dn, s, "down GEMM");
+            if (split) {
+                MOE_CUDA(cudaEventRecord(p->ev_perm, s));
+                MOE_CUDA(cudaStreamWaitEvent(p->side, p->ev_perm, 0));
+                for (int i = 0; i < 2; ++i) {
+                    if (st == MOE_OK) st = run_gemm(p, gp[i], s, i == 0 ? "gate/up GEMM, 256-row pairs" : "down GEMM, 256-row pairs");
+                    if (side_st == MOE_OK)
+                        side_st = run_gemm(p, gr[i], p->side, i == 0 ? "gate/up GEMM, remaining rows" : "down GEMM, remaining rows");
+                }
+                MOE_CUDA(cudaEventRecord(p->ev_join, p->side));
+            } else {
+                if (st == MOE_OK) st = run_gemm(p, gu, s, "gate/up GEMM");
+                if (st == MOE_OK) st = run_gemm(p, dn, s, "down GEMM");
+            }
         }
         MOE_CUDA(cudaStreamWaitEvent(s, p->ev_join, 0));  // joined even after an error (stream capture)
         if (side_st != MOE_OK) return side_st;

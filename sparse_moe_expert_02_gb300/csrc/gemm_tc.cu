@@ -118,6 +118,7 @@ struct Params {
     int out_f16;         // SwiGLU output as fp16 (single rounding) instead of bf16
     int in_f16;          // A and B are fp16 (else bf16)
     int narrow;          // units of <= kNarrowMax valid rows run transposed (narrow tails)
+    int rem_only;        // split GEMMs: only the rows after each group's whole 256-row pairs
     int stages;          // ring depth (<= kMaxStages)
     int b_stage;         // bytes of one B stage
     void* out;
@@ -154,6 +155,7 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u, int total_ti
         r.m0 = (rt - s_tiles[r.g]) * BM;
         r.row0 = s_off[r.g];
         r.nrows = s_off[r.g + 1] - r.row0;
+        if (p.rem_only) r.m0 += 2 * BM * (r.nrows / (2 * BM));  // past the group's whole pairs
     } else {
         r.g = 0;
         r.m0 = rt * BM;
@@ -928,10 +930,11 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     p.cmb_inv = g.cmb_inv;
     p.cmb_y = g.cmb_y;
     p.cmb_k = g.cmb_k;
+    p.rem_only = g.rem_only && g.offsets;
 
     // tile pairs: whole weight blocks in pairs (SwiGLU: 128 gate + 128 up;
     // plain: 256-wide), no K split, one A input; static unit order
-    const bool cl = g.mcast && !pair && p.KS == 1 && p.NB % 2 == 0 && (sw || p.BN == 256);
+    const bool cl = g.mcast && !pair && p.KS == 1 && p.NB % 2 == 0 && (sw || p.BN == 256) && !p.rem_only;
     if (cl) p.sched = nullptr;
     // narrow tails: expert GEMMs with 16-bit outputs in whole 128-feature regions
     p.narrow = g.narrow && !pair && p.KS == 1 && !g.out_pair && !g.bias && g.out_elem != kF32 &&

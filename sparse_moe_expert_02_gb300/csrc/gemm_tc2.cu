@@ -8,8 +8,13 @@
 // tile (128 of the 256 weight rows), the pair's leader issues M=256 MMAs that
 // read both CTAs' shared memory, and each CTA's TMEM receives its own 128
 // rows x 256 columns: each SM moves about two thirds of the operand bytes per
-// MMA cycle, and the ring holds 6 stages.  (Measured at T=8192 this was no
-// faster than the single-CTA kernel, so it runs on request only.)
+// MMA cycle, and the ring holds 6 stages.  A whole 256-row pair unit runs
+// ~11 % (gate/up) to ~29 % (down) faster per SM than two single-CTA tiles,
+// but ragged pair tiles cost more than single-CTA tails, so on its own the
+// kernel is no faster at T=8192 and runs on request; at prefill sizes it
+// takes the whole 256-row pairs of the split expert GEMMs (with `active`:
+// only that many pairs work, the rest leave at once) while the single-CTA
+// kernel takes the remainders on another stream.
 //   SwiGLU: CTA 0 holds the 128 gate rows, CTA 1 the 128 up rows of the same
 //     features, so accumulator columns 0..127 are gate and 128..255 up in both.
 //   Plain: CTA r holds weight rows nb*256 + r*128 .. +127.
@@ -80,6 +85,7 @@ struct Params {
     const int32_t* tiles2;  // prefix of ceil(rows/256)
     int NB, N, KB, a_lo_x, ldo, out_pair, out_f32, out_f16, in_f16;
     int narrow;             // ragged pair tiles run transposed (16-bit outputs only)
+    const int32_t* active;  // split GEMMs: [1] CTA pairs that take units (the rest leave at once), or nullptr
     void* out;
     uint32_t* err;
     int64_t spin_ns;
@@ -213,6 +219,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* s_stage = smem + kStageOff;        // [4 epilogue warps][32 rows][kStRow]
     float* s_xchg = (float*)(smem + kXchgOff);  // [2 warp pairs][32 lanes][kXRow]
     pdl_wait_then_release();
+    // split GEMMs: only the first `npairs` CTA pairs take units; the others
+    // leave before touching a barrier, TMEM or the peer, and free their SMs
+    const int npairs = p.active ? min(__ldg(p.active), (int)(gridDim.x >> 1)) : (int)(gridDim.x >> 1);
+    if ((int)(blockIdx.x >> 1) >= npairs) return;
     for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
         s_t2[i] = __ldg(p.tiles2 + i);
         s_off[i] = __ldg(p.offsets + i);
@@ -243,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
-    const int nclusters = gridDim.x >> 1, cid = blockIdx.x >> 1;
+    const int nclusters = npairs, cid = blockIdx.x >> 1;
     const int total_units = s_t2[p.g_end] * p.NB;
     const int64_t lim = p.spin_ns;
     bool aborted = false;
@@ -613,6 +623,7 @@ cudaError_t launch_gemm_tc2(const GroupedGemm& g, int num_sms, cudaStream_t stre
     p.in_f16 = g.elem == kF16;
     // narrow tails: 16-bit outputs only (the transposed stores), not the hi/lo pair input
     p.narrow = g.narrow && !pair && !g.out_pair && g.out_elem != kF32;
+    p.active = g.pair_active;
     p.out = g.out;
     p.err = g.err;
     p.spin_ns = g.spin_ns > 0 ? g.spin_ns : 2000000000LL;

@@ -42,6 +42,10 @@ struct GroupedGemm {
                                  // operand tiles by TMA multicast) where the shape allows them
     int narrow;                  // bf16/fp16 tensor-core kernel: 1 = tiles of <= 112 valid rows multiplied
                                  // transposed (weights as M, rows as N rounded up to 16)
+    int rem_only;                // bf16 single-CTA kernel, split GEMMs: `tiles` counts the 128-row tiles
+                                 // left after each group's whole 256-row pairs, which start its rows
+    const int32_t* pair_active;  // CTA-pair kernel, split GEMMs: [1] device count of CTA pairs that work
+                                 // (the rest exit at once); its units are whole 256-row pairs (tiles2)
     int many_rows;               // FP8 kernel: groups hold many rows (prefill sizes): stage the down
                                  // GEMM's y stores through shared memory
     int rows;                    // single-group row count
@@ -161,9 +165,13 @@ cudaError_t launch_pack_words(const int32_t* blob, int64_t TK, int32_t* words, c
 // pairs of the two-CTA GEMM.
 // hist_ready: the per-chunk histograms were already counted (by the top-k
 // kernel) -- only meaningful where permute_uses_chunks().
+// pairs (nullable): the split expert GEMMs' tile prefixes and CTA-pair counts
+// ([2, E+2] + [2], see moe_ws_layout::pairs) for `clusters` CTA pairs at
+// most; narrow_gu: the gate/up GEMM's ragged tiles run as narrow tails.
 cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_t* hist, int32_t* counts,
                                  int32_t* offsets, int32_t* tiles, int32_t* tiles2, int32_t* inv, int32_t* src_tok,
-                                 uint32_t* err, cudaStream_t stream, bool hist_ready = false);
+                                 uint32_t* err, cudaStream_t stream, bool hist_ready = false, int32_t* pairs = nullptr,
+                                 int clusters = 0, int narrow_gu = 0);
 // Whether T*k pairs over E experts take the chunked permutation (per-chunk
 // histograms in the workspace) rather than the single-block one.
 bool permute_uses_chunks(int64_t TK, int E);

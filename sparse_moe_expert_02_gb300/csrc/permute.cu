@@ -78,12 +78,75 @@ __device__ void warp_exclusive_scan(const int32_t* v, int n, int32_t* out) {
     if (lane == 31) out[n] = incl;
 }
 
+// Split expert GEMMs (bf16 layer at prefill sizes): for every group the
+// whole 256-row pairs (CTA-pair launch) and the 128-row tiles of the rest
+// (single-CTA launch, concurrent on the second stream), written as exclusive
+// prefixes to pairs[0 .. E+1] and pairs[E+2 .. 2E+3]; then the number of CTA
+// pairs each GEMM's pair launch keeps (gate/up, down), in proportion to its
+// share of the work.  The work is counted in SM cycles per k-block as
+// measured on the bf16 prefill layer (T=8192, E=512): a pair k-block
+// (256 rows, one on each SM) 626 / 633 cycles per SM (gate/up / down), a
+// single-CTA 128-row k-block 703 / 889, a narrow (transposed) tail of at most
+// 112 rows 1,063 (gate/up only; they stream the whole weight block for few
+// rows).  A pair count off this balance leaves one launch waiting for the
+// other: T=8192 took 2.67 ms with 56 pairs against 76, 2.14 with 48, 2.36 with
+// 40, against 2.22 ms for the single-CTA kernel alone.
+constexpr float kCostPairGU = 626.f, kCostPairDN = 633.f, kCostFullGU = 703.f, kCostFullDN = 889.f,
+                kCostNarrowGU = 1063.f;
+// cnt: [E+1] rows per group (shared group last) in shared memory; s_f, s_r:
+// [E+1] shared scratch; s_red: [32 * 4] floats.  Every thread of the block
+// calls it.
+__device__ void pair_split(const int32_t* cnt, int E, int32_t* s_f, int32_t* s_r, float* s_red, int32_t* pairs,
+                           int clusters, int narrow_gu) {
+    float w[4] = {0.f, 0.f, 0.f, 0.f};  // pair / rest work of gate/up, then down
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        const int n = cnt[e];
+        const int f = n / (2 * kRowTile), r = n % (2 * kRowTile);
+        const int rf = r / kRowTile, rt = r % kRowTile;
+        s_f[e] = f;
+        s_r[e] = rf + (rt > 0);
+        if (e < E) {
+            w[0] += 2.f * kCostPairGU * f;
+            w[1] += kCostFullGU * rf + (rt ? ((narrow_gu && rt <= 112) ? kCostNarrowGU : kCostFullGU) : 0.f);
+            w[2] += 2.f * kCostPairDN * f;
+            w[3] += kCostFullDN * (rf + (rt > 0));
+        }
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) w[j] += __shfl_xor_sync(0xffffffffu, w[j], o);
+        if (lane == 0) s_red[warp * 4 + j] = w[j];
+    }
+    __syncthreads();
+    const int nw = blockDim.x >> 5;
+    if (warp == 4) {
+        warp_exclusive_scan(s_f, E + 1, pairs);
+    } else if (warp == 5) {
+        warp_exclusive_scan(s_r, E + 1, pairs + (E + 2));
+    } else if (threadIdx.x == 192) {
+        float t[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int i = 0; i < nw; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) t[j] += s_red[i * 4 + j];
+        for (int g = 0; g < 2; ++g) {
+            const float a = t[2 * g], b = t[2 * g + 1];
+            const int c = (a + b > 0.f) ? (int)lrintf((float)clusters * a / (a + b)) : 0;
+            pairs[2 * (E + 2) + g] = min(clusters, max(0, c));
+        }
+    }
+}
+
 __global__ void __launch_bounds__(512) perm_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E, int T,
                                                          int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                                                          int32_t* __restrict__ tiles, int32_t* __restrict__ tiles2,
-                                                         int32_t* __restrict__ shared_src, int64_t TK) {
+                                                         int32_t* __restrict__ shared_src, int64_t TK,
+                                                         int32_t* __restrict__ pairs, int clusters, int narrow_gu) {
     pdl_wait_then_release();
     __shared__ int32_t cnt[1025 + 1];
+    __shared__ int32_t s_pf[1025 + 1], s_pr[1025 + 1];
+    __shared__ float s_red[32 * 4];
     __shared__ int32_t ntile[1025 + 1];
     __shared__ int32_t ntile2[1025 + 1];
     // the shared expert's rows: token t at grouped row T*k + t
@@ -114,6 +177,7 @@ __global__ void __launch_bounds__(512) perm_scan_kernel(int32_t* __restrict__ hi
         ntile2[E] = (T + 2 * kRowTile - 1) / (2 * kRowTile);
     }
     __syncthreads();
+    if (pairs) pair_split(cnt, E, s_pf, s_pr, s_red, pairs, clusters, narrow_gu);
     for (int e = threadIdx.x; e <= E; e += blockDim.x) counts[e] = cnt[e];
     if (threadIdx.x < 32) warp_exclusive_scan(cnt, E + 1, offsets);
     else if (threadIdx.x < 64) warp_exclusive_scan(ntile, E + 1, tiles);
@@ -197,14 +261,16 @@ __global__ void __launch_bounds__(32 * kRankWarps) perm_rank_kernel(const int32_
 // of four dependent launches.
 constexpr int kSmallPairs = 16384;
 constexpr int kSmallMaxE = 512;
-constexpr int kSmallSmem = (32 * kSmallMaxE + 4 * (kSmallMaxE + 2)) * 4;
+constexpr int kSmallSmem = (32 * kSmallMaxE + 6 * (kSmallMaxE + 2) + 32 * 4) * 4;
 
 __global__ void __launch_bounds__(1024) perm_index_small_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
                                                                 int32_t* __restrict__ counts,
                                                                 int32_t* __restrict__ offsets,
                                                                 int32_t* __restrict__ tiles,
                                                                 int32_t* __restrict__ tiles2, int32_t* __restrict__ inv,
-                                                                int32_t* __restrict__ src_tok, uint32_t* err) {
+                                                                int32_t* __restrict__ src_tok, uint32_t* err,
+                                                                int32_t* __restrict__ pairs, int clusters,
+                                                                int narrow_gu) {
     pdl_wait_then_release();
     extern __shared__ int32_t sm[];
     int32_t* hist = sm;                   // [32][E]: per-warp counts, then cursors
@@ -212,6 +278,9 @@ __global__ void __launch_bounds__(1024) perm_index_small_kernel(const int32_t* _
     int32_t* nt = cnt + (E + 2);          // [E+1] 128-row tiles
     int32_t* nt2 = nt + (E + 2);          // [E+1] 256-row tiles
     int32_t* off = nt2 + (E + 2);         // [E+2]
+    int32_t* s_pf = off + (E + 2);        // [E+1] pair split scratch
+    int32_t* s_pr = s_pf + (E + 2);       // [E+1]
+    float* s_red = (float*)(s_pr + (E + 2));  // [32 * 4]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int TK = T * k;
     const int per = (TK + 31) / 32;
@@ -242,6 +311,7 @@ __global__ void __launch_bounds__(1024) perm_index_small_kernel(const int32_t* _
         nt2[E] = (T + 2 * kRowTile - 1) / (2 * kRowTile);
     }
     __syncthreads();
+    if (pairs) pair_split(cnt, E, s_pf, s_pr, s_red, pairs, clusters, narrow_gu);
     if (warp == 0) warp_exclusive_scan(cnt, E + 1, off);
     else if (warp == 1) warp_exclusive_scan(nt, E + 1, tiles);
     else if (warp == 2 && tiles2) warp_exclusive_scan(nt2, E + 1, tiles2);
@@ -276,14 +346,15 @@ bool permute_uses_chunks(int64_t TK, int E) { return !(TK <= kSmallPairs && E <=
 
 cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_t* hist, int32_t* counts,
                                  int32_t* offsets, int32_t* tiles, int32_t* tiles2, int32_t* inv, int32_t* src_tok,
-                                 uint32_t* err, cudaStream_t stream, bool hist_ready) {
+                                 uint32_t* err, cudaStream_t stream, bool hist_ready, int32_t* pairs, int clusters,
+                                 int narrow_gu) {
     const int64_t TK = (int64_t)T * k;
     if (!permute_uses_chunks(TK, E)) {
         cudaError_t e = ensure_smem_attr((const void*)perm_index_small_kernel, kSmallSmem);
         if (e != cudaSuccess) return e;
-        const int smem = (32 * E + 4 * (E + 2)) * 4;
+        const int smem = (32 * E + 6 * (E + 2) + 32 * 4) * 4;
         e = launch_kernel(perm_index_small_kernel, dim3(1), dim3(1024), smem, stream, 1, idx, T, E, k, counts, offsets,
-                          tiles, tiles2, inv, src_tok, err);
+                          tiles, tiles2, inv, src_tok, err, pairs, clusters, narrow_gu);
         count_launches(1);
         return e != cudaSuccess ? e : cudaGetLastError();
     }
@@ -293,7 +364,7 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
         e = launch_kernel(perm_hist_kernel, dim3(nch), dim3(256), E * sizeof(int32_t), stream, 1, idx, TK, E, hist, err);
     if (e == cudaSuccess)
         e = launch_kernel(perm_scan_kernel, dim3(1), dim3(512), 0, stream, 1, hist, nch, E, T, counts, offsets, tiles,
-                          tiles2, src_tok, TK);
+                          tiles2, src_tok, TK, pairs, clusters, narrow_gu);
     if (e != cudaSuccess) return e;
     const int rank_smem = kRankWarps * E * (int)sizeof(int32_t);
     if (rank_smem > 48 * 1024) {

@@ -686,3 +686,48 @@ def test_fused_unpermutation_is_bit_identical(shape, flags, out_dtype):
         fused.check()
     torch.cuda.synchronize()
     assert torch.equal(out_f, out_p)
+
+
+@pytest.mark.parametrize("shape", [synth.SMALL_BF16.with_tokens(700), synth.SMALL_BF16.with_tokens(2000),
+                                   synth.LayerShape("bf16_uniform_T3000_D512_E32_I256_k4", 3000, 512, 32, 256, 4, "bf16"),
+                                   synth.SMALL_BF16.with_tokens(129)],
+                         ids=["T700", "T2000", "uniform_T3000", "T129_unsplit"])
+def test_split_expert_gemms_are_bit_identical(shape):
+    """Split expert GEMMs (prefill sizes): whole 256-row pairs on CTA pairs,
+    the rest of each group on single CTAs, concurrently -- the same output
+    bit for bit as one launch per GEMM, twice in a row, and within tolerance
+    of the oracle; the CTA-pair counts the permutation chose lie in range."""
+    inp = _dev_inputs(shape, seed=17)
+    whole = MoELayer.from_shape(shape, inp, flags=L.MOE_FLAG_SPLIT_GEMM_OFF)
+    out_w = whole.forward(inp["x"])
+    whole.check()
+    layer, out_s, _ = _layer_parity(shape, inp, rows=sample_rows(shape.T, 32, seed=8))
+    out_s2 = layer.forward(inp["x"])
+    layer.check()
+    torch.cuda.synchronize()
+    assert torch.equal(out_s, out_w) and torch.equal(out_s2, out_w)
+    E = shape.E
+    pairs = layer.ws_view(shape.T, "pairs", torch.int32, (2 * (E + 2) + 2,)).cpu().numpy()
+    counts = layer.views(shape.T)["counts"].cpu().numpy()[:E]
+    assert np.array_equal(np.diff(pairs[:E + 1]), counts // 256)
+    assert np.array_equal(np.diff(pairs[E + 2:2 * E + 3]), (counts % 256 + 127) // 128)
+    assert 0 <= pairs[-2] <= 76 and 0 <= pairs[-1] <= 76
+
+
+def test_split_expert_gemms_at_full_prefill_size(big_bf16_weights):
+    """The 8K-token prefill layer with and without the split: bit-identical."""
+    w_dev, _ = big_bf16_weights
+    shape = synth.PREFILL_BF16
+    inp = _dev_inputs(shape, seed=0, weights=False)
+    inp.update(w_dev)
+    split = MoELayer.from_shape(shape, inp, out_dtype="bf16")
+    whole = MoELayer.from_shape(shape, inp, flags=L.MOE_FLAG_SPLIT_GEMM_OFF, out_dtype="bf16")
+    a = split.forward(inp["x"])
+    b = whole.forward(inp["x"])
+    split.check()
+    whole.check()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    E = shape.E
+    pairs = split.ws_view(shape.T, "pairs", torch.int32, (2 * (E + 2) + 2,)).cpu().numpy()
+    assert 0 < pairs[-2] < 76 and 0 < pairs[-1] < 76   # skewed routing: both launches have work
