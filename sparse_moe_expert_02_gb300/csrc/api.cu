@@ -673,6 +673,23 @@ bool split_wanted(const moe_plan* p, int T, Ws& W, const moe::GroupedGemm& gu, c
     return true;
 }
 
+// A stage entry point's expert GEMM (all groups, the shared one included),
+// split as in moe_forward where that applies: the whole 256-row pairs on the
+// caller's stream, the rest on the plan's second stream, joined back before
+// returning.  which: 0 gate/up, 1 down.
+moe_status run_stage_gemm(const moe_plan* p, const moe::GroupedGemm& g, int which, int32_t T, Ws& W, cudaStream_t s,
+                          const char* what) {
+    moe::GroupedGemm gp[2], gr[2];
+    if (!split_wanted(p, T, W, g, g, gp, gr)) return run_gemm(p, g, s, what);
+    MOE_CUDA(cudaEventRecord(p->ev_fork, s));
+    MOE_CUDA(cudaStreamWaitEvent(p->side, p->ev_fork, 0));
+    const moe_status st = run_gemm(p, gp[which], s, what);
+    const moe_status st2 = run_gemm(p, gr[which], p->side, what);
+    MOE_CUDA(cudaEventRecord(p->ev_join, p->side));
+    MOE_CUDA(cudaStreamWaitEvent(s, p->ev_join, 0));  // joined even after an error (stream capture)
+    return st != MOE_OK ? st : st2;
+}
+
 }  // namespace
 
 moe_status moe_gemm_gateup(const moe_plan* p, const moe_weights* w, const void* x, int32_t T, void* ws,
@@ -682,7 +699,7 @@ moe_status moe_gemm_gateup(const moe_plan* p, const moe_weights* w, const void* 
     if (st != MOE_OK) return st;
     if ((st = check_weights(p, w, false, true)) != MOE_OK) return st;
     if (!ptr_ok(x)) return arg_fail(MOE_ERR_INVALID_ARG, "x NULL or misaligned");
-    return run_gemm(p, gateup_gemm(p, w, x, T, W), (cudaStream_t)stream, "gate/up GEMM");
+    return run_stage_gemm(p, gateup_gemm(p, w, x, T, W), 0, T, W, (cudaStream_t)stream, "gate/up GEMM");
 }
 
 moe_status moe_gemm_down(const moe_plan* p, const moe_weights* w, int32_t T, void* ws, size_t ws_bytes,
@@ -691,7 +708,7 @@ moe_status moe_gemm_down(const moe_plan* p, const moe_weights* w, int32_t T, voi
     moe_status st = check_call(p, T, ws, ws_bytes, &W);
     if (st != MOE_OK) return st;
     if ((st = check_weights(p, w, false, true)) != MOE_OK) return st;
-    return run_gemm(p, down_gemm(p, w, T, W), (cudaStream_t)stream, "down GEMM");
+    return run_stage_gemm(p, down_gemm(p, w, T, W), 1, T, W, (cudaStream_t)stream, "down GEMM");
 }
 
 moe_status moe_unpermute(const moe_plan* p, int32_t T, void* out, void* ws, size_t ws_bytes, void* stream) {

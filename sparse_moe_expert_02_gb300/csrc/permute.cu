@@ -90,9 +90,13 @@ __device__ void warp_exclusive_scan(const int32_t* v, int n, int32_t* out) {
 // 112 rows 1,063 (gate/up only; they stream the whole weight block for few
 // rows).  A pair count off this balance leaves one launch waiting for the
 // other: T=8192 took 2.67 ms with 56 pairs against 76, 2.14 with 48, 2.36 with
-// 40, against 2.22 ms for the single-CTA kernel alone.
+// 40, against 2.22 ms for the single-CTA kernel alone.  The pair side's work
+// is weighted up by kPairBias: the single-CTA launch starts after the shared
+// expert's GEMMs on its stream, and too few pairs cost far more than too
+// many (pair work scaled by 0.85: 2.31 ms; 1.0: 2.14 - 2.17; 1.15: 2.10; 1.3:
+// 2.11).
 constexpr float kCostPairGU = 626.f, kCostPairDN = 633.f, kCostFullGU = 703.f, kCostFullDN = 889.f,
-                kCostNarrowGU = 1063.f;
+                kCostNarrowGU = 1063.f, kPairBias = 1.2f;
 // cnt: [E+1] rows per group (shared group last) in shared memory; s_f, s_r:
 // [E+1] shared scratch; s_red: [32 * 4] floats.  Every thread of the block
 // calls it.
@@ -131,7 +135,7 @@ __device__ void pair_split(const int32_t* cnt, int E, int32_t* s_f, int32_t* s_r
 #pragma unroll
             for (int j = 0; j < 4; ++j) t[j] += s_red[i * 4 + j];
         for (int g = 0; g < 2; ++g) {
-            const float a = t[2 * g], b = t[2 * g + 1];
+            const float a = t[2 * g] * kPairBias, b = t[2 * g + 1];
             const int c = (a + b > 0.f) ? (int)lrintf((float)clusters * a / (a + b)) : 0;
             pairs[2 * (E + 2) + g] = min(clusters, max(0, c));
         }

@@ -200,7 +200,8 @@ def test_forward_replays_from_a_cuda_graph(shape):
 
 
 @pytest.mark.parametrize("shape,T", [(synth.SMALL_BF16, 300), (synth.SMALL_BF16, 1), (synth.SMALL_FP8, 300),
-                                     (synth.SMALL_FP8, 129)], ids=["bf16_300", "bf16_1", "fp8_300", "fp8_129"])
+                                     (synth.SMALL_FP8, 129), (synth.SMALL_BF16, 2000)],
+                         ids=["bf16_300", "bf16_1", "fp8_300", "fp8_129", "bf16_2000_split_gemms"])
 def test_forward_equals_stage_pipeline(shape, T):
     """moe_forward runs the shared expert as its own GEMMs on a second stream
     and the routed GEMMs over the routed groups only; the stage entry points
