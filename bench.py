@@ -151,17 +151,23 @@ def algorithmic(shape, counts: np.ndarray):
 
 
 def traffic_for(kernel: str, workload: str):
-    """dram bytes per launch from the committed ncu summary, if it was taken
-    on the kernel source as it stands now (else null)."""
+    """dram bytes of the stage (per launch; summed over its launches where a
+    GEMM is split) from the committed ncu summary, if it was taken on the
+    kernel sources as they stand now (else null)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
         ent = d[workload][kernel]
-        src = os.path.join(ROOT, "sparse_moe_expert_02_gb300", "csrc", ent["source_file"])
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        return ent["dram_bytes_per_launch"] if h == ent["source_sha"] else None
+        # a stage run as several launches (split GEMMs) lists every source
+        files = ent.get("source_files") or [ent["source_file"]]
+        shas = ent.get("source_shas") or [ent["source_sha"]]
+        for f, want in zip(files, shas):
+            src = os.path.join(ROOT, "sparse_moe_expert_02_gb300", "csrc", f)
+            if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != want:
+                return None
+        return ent["dram_bytes_per_launch"]
     except Exception:
         return None
 
