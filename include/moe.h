@@ -210,10 +210,13 @@ typedef struct moe_ws_layout {
                           fp16 (MOE_BF16) or bf16 (FP8 layer) */
     size_t logits_part;/* f32 [S, T, E] router K-slice partials when T is small (S > 1), else 0 */
     size_t tiles2;     /* int32 [E+2]: exclusive prefix of ceil(counts/256) (row-tile pairs) */
-    size_t pairs;      /* int32 [2, E+2] then [2]: exclusive prefixes of floor(counts/256) (whole
-                          256-row pairs) and of the 128-row tiles of what remains of each group,
-                          then the CTA-pair clusters the split expert GEMMs run with (gate/up,
-                          down); written by the permutation (see MOE_FLAG_SPLIT_GEMM_OFF) */
+    size_t pairs;      /* int32 [2, E+2], [2], [E+2]: the exclusive prefix of floor(counts/256)
+                          by group (whole 256-row pairs); the exclusive prefix of the 128-row
+                          tiles of what remains of each group, taken over the positions of
+                          the order below; the CTA-pair clusters the split expert GEMMs run
+                          with (gate/up, down); the group at each position of the single-CTA
+                          launch's order (a permutation of 0..E, the shared group E last).
+                          Written by the permutation (see MOE_FLAG_SPLIT_GEMM_OFF) */
 } moe_ws_layout;
 
 /* Validate a configuration and build a host-side plan for `device`.

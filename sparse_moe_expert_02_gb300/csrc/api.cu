@@ -145,7 +145,7 @@ void layout(const moe_config& c, int num_sms, int T, moe_ws_layout* L) {
     const int S = route_splits(c, T, num_sms);
     L->logits_part = S > 1 ? take((size_t)S * T * c.E * 4) : 0;
     L->tiles2 = take((size_t)(c.E + 2) * 4);
-    L->pairs = take((size_t)(2 * (c.E + 2) + 2) * 4);
+    L->pairs = take((size_t)(3 * (c.E + 2) + 2) * 4);
     L->total = o;
 }
 
@@ -647,8 +647,9 @@ moe::GroupedGemm shared_only(const moe::GroupedGemm& full, const moe_config& c, 
 // off.  Fills the two launches of each GEMM: gp on CTA pairs over the whole
 // 256-row pairs (pairs[0..E+1]), as many pairs as the permutation counted
 // (pairs[2(E+2) + i]); gr on single CTAs over the rest of each group
-// (pairs[E+2..]), drawing units from the shared expert's counters (its GEMMs
-// are done by then on the same stream).
+// (pairs[E+2..], in the group order at pairs[2(E+2)+2..] that keeps it near
+// the pair launch's progress), drawing units from the shared expert's
+// counters (its GEMMs are done by then on the same stream).
 bool split_wanted(const moe_plan* p, int T, Ws& W, const moe::GroupedGemm& gu, const moe::GroupedGemm& dn,
                   moe::GroupedGemm* gp, moe::GroupedGemm* gr) {
     const moe_config& c = p->cfg;
@@ -665,6 +666,7 @@ bool split_wanted(const moe_plan* p, int T, Ws& W, const moe::GroupedGemm& gu, c
         gr[i] = base;
         gr[i].tiles = pairs + (c.E + 2);
         gr[i].rem_only = 1;
+        gr[i].rem_order = pairs + 2 * (c.E + 2) + 2;
         gr[i].mcast = 0;
         gr[i].prefer_pairs = 0;
         gr[i].sched = W.sched(i == 0 ? kSchedSharedGateup : kSchedSharedDown);

@@ -71,7 +71,8 @@ constexpr int kBoxRowsA = 16;             // a ragged tile's A rows come in 16-r
                                           // a full tile's in one 128-row box: the single
                                           // producer thread issues few TMA instructions
 // Shared-memory copy of the group row-tile prefix and row offsets (G <= 1025
-// groups): a unit's group comes from a binary search that never leaves the SM.
+// groups), and for the split GEMMs' single-CTA launch the order it takes the
+// groups in: a unit's group comes from a binary search that never leaves the SM.
 constexpr int kTabEntries = 1056;
 // Plain epilogue, 16-bit output: each epilogue warp stages 32 rows x 64
 // columns (128 B per row, rows 144 B apart: conflict-free) in shared memory
@@ -80,7 +81,7 @@ constexpr int kTabEntries = 1056;
 // (0.74 ms at T=8192, 0.62 ms with the stores left out) waited on them.
 constexpr int kStageRow = 144;
 constexpr uint32_t kStagingBytes = 4 * 32 * kStageRow;
-constexpr uint32_t kSmemBytes = 1024 + 196608 + 256 + 2 * kTabEntries * 4 + kStagingBytes;
+constexpr uint32_t kSmemBytes = 1024 + 196608 + 256 + 3 * kTabEntries * 4 + kStagingBytes;
 static_assert(kSmemBytes <= 232448, "shared memory plan exceeds 227 KB");
 
 // Stage geometry.  PAIR: A is a bf16 hi/lo pair (hi in columns [0, Kb), lo in
@@ -119,6 +120,7 @@ struct Params {
     int in_f16;          // A and B are fp16 (else bf16)
     int narrow;          // units of <= kNarrowMax valid rows run transposed (narrow tails)
     int rem_only;        // split GEMMs: only the rows after each group's whole 256-row pairs
+    const int32_t* order;  // split GEMMs: [G] group at each position of `tiles` (nullptr: position = group)
     int stages;          // ring depth (<= kMaxStages)
     int b_stage;         // bytes of one B stage
     void* out;
@@ -140,10 +142,10 @@ struct Unit {
     int g, m0, row0, nrows, nb, ks;
 };
 
-// Units: K slice major, then row tile, then feature block.  s_tiles/s_off:
-// shared copies of p.tiles and p.offsets (entries 0..G).
+// Units: K slice major, then row tile, then feature block.  s_tiles/s_off/
+// s_ord: shared copies of p.tiles and p.offsets (entries 0..G) and p.order.
 __device__ __forceinline__ Unit decode_unit(const Params& p, int u, int total_tiles, const int32_t* s_tiles,
-                                            const int32_t* s_off) {
+                                            const int32_t* s_off, const int32_t* s_ord) {
     Unit r;
     const int per_slice = total_tiles * p.NB;
     r.ks = u / per_slice;
@@ -151,8 +153,9 @@ __device__ __forceinline__ Unit decode_unit(const Params& p, int u, int total_ti
     const int rt = u / p.NB;
     r.nb = u - rt * p.NB;
     if (p.offsets) {
-        r.g = find_group_smem(s_tiles, p.G, rt);
-        r.m0 = (rt - s_tiles[r.g]) * BM;
+        const int pos = find_group_smem(s_tiles, p.G, rt);
+        r.g = p.order ? min(max(s_ord[pos], 0), p.G - 1) : pos;  // clamped against a stale table
+        r.m0 = (rt - s_tiles[pos]) * BM;
         r.row0 = s_off[r.g];
         r.nrows = s_off[r.g + 1] - r.row0;
         if (p.rem_only) r.m0 += 2 * BM * (r.nrows / (2 * BM));  // past the group's whole pairs
@@ -250,12 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = (uint64_t*)(smem + kRingBytes);
     int32_t* s_tiles = (int32_t*)(smem + kRingBytes + 256);
     int32_t* s_off = s_tiles + kTabEntries;
-    uint8_t* s_stage = (uint8_t*)(s_off + kTabEntries);  // [4 epilogue warps][32 rows][kStageRow]
+    int32_t* s_ord = s_off + kTabEntries;
+    uint8_t* s_stage = (uint8_t*)(s_ord + kTabEntries);  // [4 epilogue warps][32 rows][kStageRow]
     pdl_wait_then_release();
     if (p.offsets)
         for (int i = threadIdx.x; i <= p.G; i += blockDim.x) {
             s_tiles[i] = __ldg(p.tiles + i);
             s_off[i] = __ldg(p.offsets + i);
+            if (p.order && i < p.G) s_ord[i] = __ldg(p.order + i);
         }
     // barrier block (256 bytes): stage full/empty [kMaxStages each], TMEM
     // full/empty [2 each], drain, unit-ring full/empty [4 each], then the
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (u < 0) break;
                 int a_sh = 0;
                 const Unit un = CL ? decode_cunit(p, u, rank, total_tiles, s_tiles, s_off, a_sh)
-                                   : decode_unit(p, u, total_tiles, s_tiles, s_off);
+                                   : decode_unit(p, u, total_tiles, s_tiles, s_off, s_ord);
                 const bool sh = un.g == p.shared_group;
                 const CUtensorMap* ta = sh ? &tm_a_sh : &tm_a;
                 const CUtensorMap* taf = sh ? &tm_a_shf : &tm_af;
@@ -439,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (p.narrow) {
                     int a_sh = 0;
                     const Unit un = CL ? decode_cunit(p, u, rank, total_tiles, s_tiles, s_off, a_sh)
-                                       : decode_unit(p, u, total_tiles, s_tiles, s_off);
+                                       : decode_unit(p, u, total_tiles, s_tiles, s_off, s_ord);
                     const int valid = min(BM, un.nrows - un.m0);
                     if (valid <= kNarrowMax) nn = (valid + 15) & ~15;
                 }
@@ -527,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!got || u < 0) break;
             int a_sh = 0;
             const Unit un = CL ? decode_cunit(p, u, rank, total_tiles, s_tiles, s_off, a_sh)
-                               : decode_unit(p, u, total_tiles, s_tiles, s_off);
+                               : decode_unit(p, u, total_tiles, s_tiles, s_off, s_ord);
             int ok = 1;
             if (lane == 0) {
                 ok = mbar_wait(tfull0 + 8 * acc, acc_phase, lim, abort_flag);
@@ -931,6 +936,7 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int num_sms, cudaStream_t strea
     p.cmb_y = g.cmb_y;
     p.cmb_k = g.cmb_k;
     p.rem_only = g.rem_only && g.offsets;
+    p.order = p.rem_only ? g.rem_order : nullptr;
 
     // tile pairs: whole weight blocks in pairs (SwiGLU: 128 gate + 128 up;
     // plain: 256-wide), no K split, one A input; static unit order

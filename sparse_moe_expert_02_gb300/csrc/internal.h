@@ -46,6 +46,8 @@ struct GroupedGemm {
                                  // left after each group's whole 256-row pairs, which start its rows
     const int32_t* pair_active;  // CTA-pair kernel, split GEMMs: [1] device count of CTA pairs that work
                                  // (the rest exit at once); its units are whole 256-row pairs (tiles2)
+    const int32_t* rem_order;    // with rem_only: [G] device group at each position of `tiles` (the
+                                 // prefix runs over positions), or nullptr for group order
     int many_rows;               // FP8 kernel: groups hold many rows (prefill sizes): stage the down
                                  // GEMM's y stores through shared memory
     int rows;                    // single-group row count

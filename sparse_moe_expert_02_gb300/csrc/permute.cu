@@ -80,40 +80,73 @@ __device__ void warp_exclusive_scan(const int32_t* v, int n, int32_t* out) {
 
 // Split expert GEMMs (bf16 layer at prefill sizes): for every group the
 // whole 256-row pairs (CTA-pair launch) and the 128-row tiles of the rest
-// (single-CTA launch, concurrent on the second stream), written as exclusive
-// prefixes to pairs[0 .. E+1] and pairs[E+2 .. 2E+3]; then the number of CTA
-// pairs each GEMM's pair launch keeps (gate/up, down), in proportion to its
-// share of the work.  The work is counted in SM cycles per k-block as
-// measured on the bf16 prefill layer (T=8192, E=512): a pair k-block
-// (256 rows, one on each SM) 626 / 633 cycles per SM (gate/up / down), a
-// single-CTA 128-row k-block 703 / 889, a narrow (transposed) tail of at most
-// 112 rows 1,063 (gate/up only; they stream the whole weight block for few
-// rows).  A pair count off this balance leaves one launch waiting for the
-// other: T=8192 took 2.67 ms with 56 pairs against 76, 2.14 with 48, 2.36 with
-// 40, against 2.22 ms for the single-CTA kernel alone.  The pair side's work
-// is weighted up by kPairBias: the single-CTA launch starts after the shared
-// expert's GEMMs on its stream, and too few pairs cost far more than too
-// many (pair work scaled by 0.85: 2.31 ms; 1.0: 2.14 - 2.17; 1.15: 2.10; 1.3:
-// 2.11).
+// (single-CTA launch, concurrent on the second stream).  pairs[0 .. E+1]:
+// exclusive prefix of the pairs by group; pairs[2(E+2) .. +1]: the number of
+// CTA pairs each GEMM's pair launch keeps (gate/up, down), in proportion to
+// its share of the work; pairs[2(E+2)+2 .. 3E+4]: the order in which the
+// single-CTA launch takes the groups (position -> group), and
+// pairs[E+2 .. 2E+3] the exclusive prefix of the rest tiles over those
+// positions.
+//
+// The work is counted in SM cycles per k-block as measured on the bf16
+// prefill layer (T=8192, E=512): a pair k-block (256 rows, one on each SM)
+// 626 / 633 cycles per SM (gate/up / down), a single-CTA 128-row k-block
+// 703 / 889, a narrow (transposed) tail of at most 112 rows 1,063 (gate/up
+// only; they stream the whole weight block for few rows).  A pair count off
+// this balance leaves one launch waiting for the other: T=8192 took 2.67 ms
+// with 56 pairs against 76, 2.14 with 48, 2.36 with 40, against 2.22 ms for
+// the single-CTA kernel alone.  The pair side's work is weighted up by
+// kPairBias: the single-CTA launch starts after the shared expert's GEMMs on
+// its stream, and too few pairs cost far more than too many (pair work scaled
+// by 0.85: 2.31 ms; 1.0: 2.14 - 2.17; 1.15: 2.10; 1.3: 2.11).
+//
+// The order: a group with both pairs and a rest has its weights read by both
+// launches.  Taken in group order, the single-CTA launch (one or two tiles a
+// group) runs far ahead of the pair launch and reads them again from DRAM.
+// So a group with pairs comes where the pair launch is halfway through it
+// (the midpoint of its pairs as a fraction of all routed pairs), a group with
+// only a rest where its midpoint falls among those groups' rest tiles; the
+// two lists are merged by that fraction (pair groups first on equal
+// fractions), the routed groups without a rest follow in group order and the
+// shared group comes last, so that positions [0, E) are the routed groups.
 constexpr float kCostPairGU = 626.f, kCostPairDN = 633.f, kCostFullGU = 703.f, kCostFullDN = 889.f,
                 kCostNarrowGU = 1063.f, kPairBias = 1.2f;
+__device__ __forceinline__ int rest_tiles(int n) { return (n % (2 * kRowTile) + kRowTile - 1) / kRowTile; }
+// Entries of sorted[0, n) below key (strict) or at most key (!strict).
+__device__ __forceinline__ int count_below(const float* sorted, int n, float key, bool strict) {
+    int lo = 0, hi = n;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (strict ? sorted[mid] < key : sorted[mid] <= key) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
+}
 // cnt: [E+1] rows per group (shared group last) in shared memory; s_f, s_r:
-// [E+1] shared scratch; s_red: [32 * 4] floats.  Every thread of the block
-// calls it.
-__device__ void pair_split(const int32_t* cnt, int E, int32_t* s_f, int32_t* s_r, float* s_red, int32_t* pairs,
-                           int clusters, int narrow_gu) {
+// [E+2] shared scratch; s_x: [4 (E+2)] shared scratch; s_red: [32 * 4]
+// floats.  Every thread of a block of at least 288 threads calls it.
+__device__ void pair_split(const int32_t* cnt, int E, int32_t* s_f, int32_t* s_r, int32_t* s_x, float* s_red,
+                           int32_t* pairs, int clusters, int narrow_gu) {
+    const int S = E + 2;
+    int32_t* x_rb = s_x;           // rest tiles of the groups with no pairs
+    int32_t* x_cls = s_x + S;      // 1: pairs and a rest; 1 << 16: a rest only
+    int32_t* x_rbp = s_x + 2 * S;  // exclusive prefix of x_rb
+    int32_t* x_clp = s_x + 3 * S;  // exclusive prefix of x_cls: (pairs-and-rest, rest-only) groups before
     float w[4] = {0.f, 0.f, 0.f, 0.f};  // pair / rest work of gate/up, then down
     for (int e = threadIdx.x; e <= E; e += blockDim.x) {
         const int n = cnt[e];
         const int f = n / (2 * kRowTile), r = n % (2 * kRowTile);
         const int rf = r / kRowTile, rt = r % kRowTile;
+        const int rest = rf + (rt > 0);
         s_f[e] = f;
-        s_r[e] = rf + (rt > 0);
+        const bool both = e < E && f > 0 && rest > 0, only = e < E && f == 0 && rest > 0;
+        x_rb[e] = only ? rest : 0;
+        x_cls[e] = (both ? 1 : 0) | (only ? 1 << 16 : 0);
         if (e < E) {
             w[0] += 2.f * kCostPairGU * f;
             w[1] += kCostFullGU * rf + (rt ? ((narrow_gu && rt <= 112) ? kCostNarrowGU : kCostFullGU) : 0.f);
             w[2] += 2.f * kCostPairDN * f;
-            w[3] += kCostFullDN * (rf + (rt > 0));
+            w[3] += kCostFullDN * rest;
         }
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -128,8 +161,12 @@ __device__ void pair_split(const int32_t* cnt, int E, int32_t* s_f, int32_t* s_r
     if (warp == 4) {
         warp_exclusive_scan(s_f, E + 1, pairs);
     } else if (warp == 5) {
-        warp_exclusive_scan(s_r, E + 1, pairs + (E + 2));
-    } else if (threadIdx.x == 192) {
+        warp_exclusive_scan(x_rb, E + 1, x_rbp);
+    } else if (warp == 6) {
+        warp_exclusive_scan(x_cls, E + 1, x_clp);
+    } else if (warp == 7) {
+        warp_exclusive_scan(s_f, E + 1, s_r);  // the pair prefix, kept in shared memory
+    } else if (threadIdx.x == 256) {
         float t[4] = {0.f, 0.f, 0.f, 0.f};
         for (int i = 0; i < nw; ++i)
 #pragma unroll
@@ -137,9 +174,37 @@ __device__ void pair_split(const int32_t* cnt, int E, int32_t* s_f, int32_t* s_r
         for (int g = 0; g < 2; ++g) {
             const float a = t[2 * g] * kPairBias, b = t[2 * g + 1];
             const int c = (a + b > 0.f) ? (int)lrintf((float)clusters * a / (a + b)) : 0;
-            pairs[2 * (E + 2) + g] = min(clusters, max(0, c));
+            pairs[2 * S + g] = min(clusters, max(0, c));
         }
     }
+    __syncthreads();
+    // the two lists' fractions, each ascending in group order (x_rb and
+    // x_cls were consumed by the scans above)
+    const int nA = x_clp[E] & 0xFFFF, nB = x_clp[E] >> 16;
+    const float pf2 = 2.f * (float)max(1, s_r[E]), rb2 = 2.f * (float)max(1, x_rbp[E]);
+    float* kA = (float*)x_rb;
+    float* kB = (float*)x_cls;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int n = cnt[e], rest = rest_tiles(n);
+        if (rest == 0) continue;
+        if (n >= 2 * kRowTile) kA[x_clp[e] & 0xFFFF] = (2.f * (float)s_r[e] + (float)(n / (2 * kRowTile))) / pf2;
+        else kB[x_clp[e] >> 16] = (2.f * (float)x_rbp[e] + (float)rest) / rb2;
+    }
+    __syncthreads();
+    int32_t* order = pairs + 2 * S + 2;
+    for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+        const int n = cnt[e], rest = rest_tiles(n);
+        const int ia = x_clp[e] & 0xFFFF, ib = x_clp[e] >> 16;
+        int pos;
+        if (e == E) pos = E;
+        else if (rest == 0) pos = nA + nB + (e - ia - ib);
+        else if (n >= 2 * kRowTile) pos = ia + count_below(kB, nB, kA[ia], true);
+        else pos = ib + count_below(kA, nA, kB[ib], false);
+        order[pos] = e;
+        s_f[pos] = rest;  // rest tiles by position (s_f's pair counts were scanned above)
+    }
+    __syncthreads();
+    if (warp == 5) warp_exclusive_scan(s_f, E + 1, pairs + S);
 }
 
 __global__ void __launch_bounds__(512) perm_scan_kernel(int32_t* __restrict__ hist, int nchunks, int E, int T,
@@ -151,6 +216,7 @@ __global__ void __launch_bounds__(512) perm_scan_kernel(int32_t* __restrict__ hi
     __shared__ int32_t cnt[1025 + 1];
     __shared__ int32_t s_pf[1025 + 1], s_pr[1025 + 1];
     __shared__ float s_red[32 * 4];
+    __shared__ int32_t s_px[4 * (1025 + 1)];
     __shared__ int32_t ntile[1025 + 1];
     __shared__ int32_t ntile2[1025 + 1];
     // the shared expert's rows: token t at grouped row T*k + t
@@ -181,7 +247,7 @@ __global__ void __launch_bounds__(512) perm_scan_kernel(int32_t* __restrict__ hi
         ntile2[E] = (T + 2 * kRowTile - 1) / (2 * kRowTile);
     }
     __syncthreads();
-    if (pairs) pair_split(cnt, E, s_pf, s_pr, s_red, pairs, clusters, narrow_gu);
+    if (pairs) pair_split(cnt, E, s_pf, s_pr, s_px, s_red, pairs, clusters, narrow_gu);
     for (int e = threadIdx.x; e <= E; e += blockDim.x) counts[e] = cnt[e];
     if (threadIdx.x < 32) warp_exclusive_scan(cnt, E + 1, offsets);
     else if (threadIdx.x < 64) warp_exclusive_scan(ntile, E + 1, tiles);
@@ -265,7 +331,7 @@ __global__ void __launch_bounds__(32 * kRankWarps) perm_rank_kernel(const int32_
 // of four dependent launches.
 constexpr int kSmallPairs = 16384;
 constexpr int kSmallMaxE = 512;
-constexpr int kSmallSmem = (32 * kSmallMaxE + 6 * (kSmallMaxE + 2) + 32 * 4) * 4;
+constexpr int kSmallSmem = (32 * kSmallMaxE + 10 * (kSmallMaxE + 2) + 32 * 4) * 4;
 
 __global__ void __launch_bounds__(1024) perm_index_small_kernel(const int32_t* __restrict__ idx, int T, int E, int k,
                                                                 int32_t* __restrict__ counts,
@@ -285,6 +351,7 @@ __global__ void __launch_bounds__(1024) perm_index_small_kernel(const int32_t* _
     int32_t* s_pf = off + (E + 2);        // [E+1] pair split scratch
     int32_t* s_pr = s_pf + (E + 2);       // [E+1]
     float* s_red = (float*)(s_pr + (E + 2));  // [32 * 4]
+    int32_t* s_px = (int32_t*)(s_red + 32 * 4);  // [4 (E+2)]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int TK = T * k;
     const int per = (TK + 31) / 32;
@@ -315,7 +382,7 @@ __global__ void __launch_bounds__(1024) perm_index_small_kernel(const int32_t* _
         nt2[E] = (T + 2 * kRowTile - 1) / (2 * kRowTile);
     }
     __syncthreads();
-    if (pairs) pair_split(cnt, E, s_pf, s_pr, s_red, pairs, clusters, narrow_gu);
+    if (pairs) pair_split(cnt, E, s_pf, s_pr, s_px, s_red, pairs, clusters, narrow_gu);
     if (warp == 0) warp_exclusive_scan(cnt, E + 1, off);
     else if (warp == 1) warp_exclusive_scan(nt, E + 1, tiles);
     else if (warp == 2 && tiles2) warp_exclusive_scan(nt2, E + 1, tiles2);
@@ -356,7 +423,7 @@ cudaError_t launch_permute_index(const int32_t* idx, int T, int E, int k, int32_
     if (!permute_uses_chunks(TK, E)) {
         cudaError_t e = ensure_smem_attr((const void*)perm_index_small_kernel, kSmallSmem);
         if (e != cudaSuccess) return e;
-        const int smem = (32 * E + 6 * (E + 2) + 32 * 4) * 4;
+        const int smem = (32 * E + 10 * (E + 2) + 32 * 4) * 4;
         e = launch_kernel(perm_index_small_kernel, dim3(1), dim3(1024), smem, stream, 1, idx, T, E, k, counts, offsets,
                           tiles, tiles2, inv, src_tok, err, pairs, clusters, narrow_gu);
         count_launches(1);

@@ -689,6 +689,37 @@ def test_fused_unpermutation_is_bit_identical(shape, flags, out_dtype):
     assert torch.equal(out_f, out_p)
 
 
+def _check_split_tables(pairs, counts, E):
+    """The split GEMMs' tables as the permutation wrote them: the pair prefix
+    by group, the single-CTA launch's group order (a permutation, routed groups
+    with a ragged rest first, merged by how far through its own launch each
+    one's midpoint lies, then the others in group order, the shared group
+    last), the rest prefix over that order, and the CTA-pair counts."""
+    S = E + 2
+    pf, rest_prefix, npairs, order = pairs[:S], pairs[S:2 * S], pairs[2 * S:2 * S + 2], pairs[2 * S + 2:2 * S + 3 + E]
+    f, rest = counts // 256, (counts % 256 + 127) // 128
+    assert np.array_equal(np.diff(pf[:E + 1]), f[:E])
+    assert np.array_equal(np.sort(order), np.arange(E + 1)) and order[E] == E
+    assert np.array_equal(np.diff(rest_prefix), rest[order])
+    assert 0 <= npairs[0] <= 76 and 0 <= npairs[1] <= 76
+    routed = order[:E]
+    has_rest = rest[routed] > 0
+    n_rest = int(has_rest.sum())
+    assert has_rest[:n_rest].all() and not has_rest[n_rest:].any()
+    assert np.all(np.diff(routed[n_rest:]) > 0)
+    a_side = f[routed[:n_rest]] > 0
+    for side in (a_side, ~a_side):
+        assert np.all(np.diff(routed[:n_rest][side]) > 0)
+    # fraction of its own launch's work at each group's midpoint, along the order
+    pfr = np.concatenate([[0], np.cumsum(f[:E])])
+    only = (f[:E] == 0) & (rest[:E] > 0)
+    rbr = np.concatenate([[0], np.cumsum(np.where(only, rest[:E], 0))])
+    g = routed[:n_rest]
+    key = np.where(f[g] > 0, (2.0 * pfr[g] + f[g]) / (2.0 * max(1, pfr[E])),
+                   (2.0 * rbr[g] + rest[g]) / (2.0 * max(1, rbr[E])))
+    assert np.all(np.diff(key) >= -1e-6)
+
+
 @pytest.mark.parametrize("shape", [synth.SMALL_BF16.with_tokens(700), synth.SMALL_BF16.with_tokens(2000),
                                    synth.LayerShape("bf16_uniform_T3000_D512_E32_I256_k4", 3000, 512, 32, 256, 4, "bf16"),
                                    synth.SMALL_BF16.with_tokens(129)],
@@ -708,11 +739,9 @@ def test_split_expert_gemms_are_bit_identical(shape):
     torch.cuda.synchronize()
     assert torch.equal(out_s, out_w) and torch.equal(out_s2, out_w)
     E = shape.E
-    pairs = layer.ws_view(shape.T, "pairs", torch.int32, (2 * (E + 2) + 2,)).cpu().numpy()
-    counts = layer.views(shape.T)["counts"].cpu().numpy()[:E]
-    assert np.array_equal(np.diff(pairs[:E + 1]), counts // 256)
-    assert np.array_equal(np.diff(pairs[E + 2:2 * E + 3]), (counts % 256 + 127) // 128)
-    assert 0 <= pairs[-2] <= 76 and 0 <= pairs[-1] <= 76
+    pairs = layer.ws_view(shape.T, "pairs", torch.int32, (3 * (E + 2) + 2,)).cpu().numpy()
+    counts = layer.views(shape.T)["counts"].cpu().numpy()
+    _check_split_tables(pairs, counts, E)
 
 
 def test_split_expert_gemms_at_full_prefill_size(big_bf16_weights):
@@ -730,5 +759,7 @@ def test_split_expert_gemms_at_full_prefill_size(big_bf16_weights):
     torch.cuda.synchronize()
     assert torch.equal(a, b)
     E = shape.E
-    pairs = split.ws_view(shape.T, "pairs", torch.int32, (2 * (E + 2) + 2,)).cpu().numpy()
-    assert 0 < pairs[-2] < 76 and 0 < pairs[-1] < 76   # skewed routing: both launches have work
+    pairs = split.ws_view(shape.T, "pairs", torch.int32, (3 * (E + 2) + 2,)).cpu().numpy()
+    _check_split_tables(pairs, split.views(shape.T)["counts"].cpu().numpy(), E)
+    S = E + 2
+    assert 0 < pairs[2 * S] < 76 and 0 < pairs[2 * S + 1] < 76   # skewed routing: both launches have work
