@@ -12,10 +12,12 @@ Parity status per function (what pins each one, see ``oracle.c`` header):
                            sum-to-one, top_k = E dense-softmax closed form
   orc_permute              pinned: counts/offsets/bijection invariants,
                            identity-expert round trip, brute-force sort
-  orc_moe_tokens / layer   pinned by invariants only: E=1,k=1 vs a numpy
-                           dense SwiGLU, identity experts, equivariances.
-                           The pages print no worked value of the layer:
-                           beyond those invariants, parity unpinned.
+  orc_moe_tokens / layer   pinned by closed forms: E=1,k=1 vs a numpy
+                           dense SwiGLU; top_k = E and (all other experts
+                           biased to zero softmax mass) top_k < E vs the
+                           dense softmax mixture in numpy/scipy; identity
+                           experts, equivariances.  The pages print no
+                           worked value of the layer.
   orc_quant_blocks         pinned: block-amax definition on planted blocks,
                            codes vs torch.float8_e4m3fn.
   quant_row_128            pinned: per-row, per-128-column amax/448 against

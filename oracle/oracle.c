@@ -33,8 +33,10 @@
  * T*k and the permutation is a bijection; token-order equivariance and
  * expert relabelling invariance; the 128x128 weight-block and the per-row
  * 128-column activation quantisers against torch's E4M3 cast, and the FP8
- * layer with one expert against numpy over that cast.  The whole-layer output has no worked value
- * in the pages: beyond these invariants it is parity unpinned.
+ * layer with one expert against numpy over that cast; the whole layer against closed forms computed
+ * with numpy and scipy: top_k = E is the dense softmax mixture, and top_k < E with every expert
+ * outside a random chosen set biased 1000 below it (zero softmax mass in fp64) is that same dense
+ * mixture.  The pages print no worked value of the layer; these closed forms pin it.
  */
 #include <math.h>
 #include <stdint.h>

@@ -312,6 +312,36 @@ def test_topk_equal_E_is_dense_softmax_mixture(dtype):
     assert np.allclose(out, ref, rtol=1e-11, atol=1e-12)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sparse_layer_is_the_dense_mixture_when_the_rest_carry_no_mass(dtype):
+    """k < E: a random set S of k experts gets router bias 0 and every other
+    expert -1000, so the full softmax gives the others exactly zero mass in
+    fp64 (exp(-1000) underflows).  The sparse layer -- choose the top k,
+    softmax over the chosen, combine -- must then equal the dense softmax
+    mixture over all E experts plus the shared expert, computed with numpy and
+    scipy.  A wrong expert chosen, a weight paired with another slot's expert
+    or a missing renormalisation all move the result."""
+    E, k = 12, 4
+    shape = synth.LayerShape("t", 10, 64, E, 32, k, dtype, 1.0)
+    inp = synth.make_inputs(shape, seed=21)
+    chosen = np.random.default_rng(5).permutation(E)[:k]
+    bias = np.full(E, -1000.0, dtype=np.float32)
+    bias[chosen] = 0.0
+    b = torch.from_numpy(bias)
+    ex = oracle.Experts(dtype, inp["w_gate"], inp["w_up"], inp["w_down"])
+    out, idx, _ = oracle.moe_layer(inp["x"], inp["w_router"], b, ex, k)
+    assert all(set(row) == set(chosen.tolist()) for row in np.asarray(idx).tolist())
+    x = inp["x"].double().numpy()
+    z = x @ inp["w_router"].double().numpy().T + bias.astype(np.float64)
+    from scipy.special import softmax
+    p = softmax(z, axis=1)
+    wg, wu, wd = (inp[n].double().numpy() for n in ("w_gate", "w_up", "w_down"))
+    ref = _np_swiglu(x, wg[E], wu[E], wd[E])
+    for e in range(E):
+        ref += p[:, e:e + 1] * _np_swiglu(x, wg[e], wu[e], wd[e])
+    assert np.allclose(out, ref, rtol=1e-11, atol=1e-12)
+
+
 def test_layer_equivariances():
     shape = synth.SMALL_F32.with_tokens(23)
     inp = synth.make_inputs(shape, seed=13)
