@@ -216,7 +216,8 @@ typedef struct moe_ws_layout {
                           the order below; the CTA-pair clusters the split expert GEMMs run
                           with (gate/up, down); the group at each position of the single-CTA
                           launch's order (a permutation of 0..E, the shared group E last).
-                          Written by the permutation (see MOE_FLAG_SPLIT_GEMM_OFF) */
+                          Written by the permutation, and only where the split can run: bf16
+                          layer, T*top_k >= 64*E (see MOE_FLAG_SPLIT_GEMM_OFF) */
 } moe_ws_layout;
 
 /* Validate a configuration and build a host-side plan for `device`.

@@ -94,6 +94,12 @@ size_t up256(size_t v) { return (v + 255) & ~(size_t)255; }
 // else h as one fp16 against an fp16 copy of W_down.
 bool hilo(const moe_config& c) { return c.dtype == MOE_BF16 && (c.flags & MOE_FLAG_DOWN_HILO); }
 bool f16_down(const moe_config& c) { return c.dtype == MOE_BF16 && !(c.flags & MOE_FLAG_DOWN_HILO); }
+// The split expert GEMMs can run for T tokens (bf16 layer at prefill sizes,
+// not turned off): only then does the permutation write their tables.
+bool split_sizes(const moe_config& c, int T) {
+    if (c.flags & (MOE_FLAG_SPLIT_GEMM_OFF | MOE_FLAG_PAIR_CTA_ON | MOE_FLAG_FORCE_SIMT)) return false;
+    return f16_down(c) && (int64_t)T * c.top_k >= 64LL * c.E;
+}
 // Expert outputs y: bf16 (FP8 layer), fp16 (bf16 layer, fp16 down path), else fp32.
 int y_elem(const moe_config& c) {
     return c.dtype == MOE_FP8_E4M3_B128 ? moe::kBF16 : f16_down(c) ? moe::kF16 : moe::kF32;
@@ -481,7 +487,8 @@ moe_status permute_impl(const moe_plan* p, const void* x, int32_t T, Ws& W, cuda
                                        W.at<int32_t>(W.L.counts), W.at<int32_t>(W.L.offsets),
                                        W.at<int32_t>(W.L.tiles), W.at<int32_t>(W.L.tiles2), W.at<int32_t>(W.L.inv),
                                        W.at<int32_t>(W.L.src_tok),
-                                       W.at<uint32_t>(W.L.err), s, hist_ready, W.at<int32_t>(W.L.pairs),
+                                       W.at<uint32_t>(W.L.err), s, hist_ready,
+                                       split_sizes(c, T) ? W.at<int32_t>(W.L.pairs) : nullptr,
                                        std::max(1, p->num_sms / 2), prefer_narrow(p, T, true)));
     if (c.dtype == MOE_FP8_E4M3_B128) {
         // xq (x quantised) is the shared expert's A operand; the routed rows
@@ -653,8 +660,7 @@ moe::GroupedGemm shared_only(const moe::GroupedGemm& full, const moe_config& c, 
 bool split_wanted(const moe_plan* p, int T, Ws& W, const moe::GroupedGemm& gu, const moe::GroupedGemm& dn,
                   moe::GroupedGemm* gp, moe::GroupedGemm* gr) {
     const moe_config& c = p->cfg;
-    if (c.flags & (MOE_FLAG_SPLIT_GEMM_OFF | MOE_FLAG_PAIR_CTA_ON | MOE_FLAG_FORCE_SIMT)) return false;
-    if (!f16_down(c) || (int64_t)T * c.top_k < 64LL * c.E) return false;
+    if (!split_sizes(c, T)) return false;
     int32_t* pairs = W.at<int32_t>(W.L.pairs);
     for (int i = 0; i < 2; ++i) {
         const moe::GroupedGemm& base = i == 0 ? gu : dn;

@@ -739,9 +739,9 @@ def test_split_expert_gemms_are_bit_identical(shape):
     torch.cuda.synchronize()
     assert torch.equal(out_s, out_w) and torch.equal(out_s2, out_w)
     E = shape.E
-    pairs = layer.ws_view(shape.T, "pairs", torch.int32, (3 * (E + 2) + 2,)).cpu().numpy()
-    counts = layer.views(shape.T)["counts"].cpu().numpy()
-    _check_split_tables(pairs, counts, E)
+    if shape.T * shape.top_k >= 64 * E:  # the permutation writes the tables only where the split runs
+        pairs = layer.ws_view(shape.T, "pairs", torch.int32, (3 * (E + 2) + 2,)).cpu().numpy()
+        _check_split_tables(pairs, layer.views(shape.T)["counts"].cpu().numpy(), E)
 
 
 def test_split_expert_gemms_at_full_prefill_size(big_bf16_weights):
