@@ -96,3 +96,32 @@ def test_our_arm_refuses_more_than_one_rank_before_loading_the_library():
     assert r.returncode != 0
     assert "one GPU only" in r.stderr and "refused before loading libmoe" in r.stderr
     assert "LIBMOE_ABSENT" in r.stdout
+
+
+def test_traffic_lookup_needs_every_source_unchanged(tmp_path, monkeypatch):
+    """roofline.traffic: the stored ncu bytes of a stage are reported only
+    while every kernel source they were taken on hashes as it did then (a
+    split stage lists two); a single-source entry works the same way."""
+    import hashlib
+    csrc = tmp_path / "sparse_moe_expert_02_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "a.cu").write_text("one")
+    (csrc / "b.cu").write_text("two")
+
+    def sha(name):
+        return hashlib.sha256((csrc / name).read_bytes()).hexdigest()[:16]
+
+    table = {"w": {"gemm_gateup": {"source_files": ["a.cu", "b.cu"], "source_shas": [sha("a.cu"), sha("b.cu")],
+                                   "dram_bytes_per_launch": 123},
+                   "gemm_down": {"source_file": "a.cu", "source_sha": sha("a.cu"), "dram_bytes_per_launch": 45}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(table))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.traffic_for("gemm_gateup", "w") == 123
+    assert bench.traffic_for("gemm_down", "w") == 45
+    assert bench.traffic_for("gemm_gateup", "other") is None
+    (csrc / "b.cu").write_text("two, edited")
+    assert bench.traffic_for("gemm_gateup", "w") is None   # one of the two sources changed
+    assert bench.traffic_for("gemm_down", "w") == 45
+    (csrc / "a.cu").write_text("one, edited")
+    assert bench.traffic_for("gemm_down", "w") is None
