@@ -97,8 +97,11 @@ __device__ void warp_exclusive_scan(const int32_t* v, int n, int32_t* out) {
 // with 56 pairs against 76, 2.14 with 48, 2.36 with 40, against 2.22 ms for
 // the single-CTA kernel alone.  The pair side's work is weighted up by
 // kPairBias: the single-CTA launch starts after the shared expert's GEMMs on
-// its stream, and too few pairs cost far more than too many (pair work scaled
-// by 0.85: 2.31 ms; 1.0: 2.14 - 2.17; 1.15: 2.10; 1.3: 2.11).
+// its stream, and too few pairs cost far more than too many.  With the group
+// order below, alternating runs on three boxes, against 1.1 (the fastest on
+// each, 2.11 - 2.13 ms per layer): 1.0 3 % slower, 1.05 up to 2 %, 1.15
+// 0.2 %, 1.2 0.5 - 0.9 %, 1.3 1.0 %, 1.45 1.3 %.  1.15 gives up 0.2 % for a
+// step of margin from the steep side.
 //
 // The order: a group with both pairs and a rest has its weights read by both
 // launches.  Taken in group order, the single-CTA launch (one or two tiles a
@@ -110,7 +113,7 @@ __device__ void warp_exclusive_scan(const int32_t* v, int n, int32_t* out) {
 // fractions), the routed groups without a rest follow in group order and the
 // shared group comes last, so that positions [0, E) are the routed groups.
 constexpr float kCostPairGU = 626.f, kCostPairDN = 633.f, kCostFullGU = 703.f, kCostFullDN = 889.f,
-                kCostNarrowGU = 1063.f, kPairBias = 1.2f;
+                kCostNarrowGU = 1063.f, kPairBias = 1.15f;
 __device__ __forceinline__ int rest_tiles(int n) { return (n % (2 * kRowTile) + kRowTile - 1) / kRowTile; }
 // Entries of sorted[0, n) below key (strict) or at most key (!strict).
 __device__ __forceinline__ int count_below(const float* sorted, int n, float key, bool strict) {
